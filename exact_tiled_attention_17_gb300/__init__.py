@@ -1,0 +1,209 @@
+"""Exact tiled attention forward for one NVIDIA GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libattn.so`` (declared in
+``include/attn.h``): the functions here only check and marshal arguments;
+every step of the computation runs in the library's CUDA kernels.  PyTorch
+provides device memory and streams.  If the library has not been built the
+import fails loudly; there is no CPU or PyTorch fallback.
+
+    attn_fwd(q, k, v, causal=False, scale=None, Br=0, Bc=0, key_mask=None)
+        -> (o, lse)          tiled exact forward (bf16 on tcgen05, or fp32 SIMT)
+    attn_naive_fwd(...)      materialising baseline (S and P in the input dtype)
+    attn_deviation(a, b)     max-abs, Wasserstein-1 (via sort), mean/std |a-b|
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+ATTN_F32, ATTN_BF16, ATTN_F64 = 0, 1, 2
+ATTN_OK = 0
+ATTN_ERR_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_WORKSPACE = -3
+ATTN_ERR_CUDA = -4
+ATTN_ERR_DEVICE_TIMEOUT = -5
+
+# Every symbol include/attn.h declares.
+EXPORTS = ("attn_fwd", "attn_naive_workspace_size", "attn_naive_fwd", "attn_deviation_workspace_size",
+           "attn_deviation", "attn_status", "attn_strerror", "attn_last_variant", "attn_debug_wait_timeout")
+
+_DTYPE = {torch.float32: ATTN_F32, torch.bfloat16: ATTN_BF16, torch.float64: ATTN_F64}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {strerror(status)} ({status})")
+        self.status = status
+
+
+class DevT(ctypes.Structure):
+    _fields_ = [("max_abs", ctypes.c_double), ("w1", ctypes.c_double), ("mean_abs", ctypes.c_double),
+                ("std_abs", ctypes.c_double), ("mean_signed", ctypes.c_double), ("n", ctypes.c_longlong)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
+                          "(the CUDA library is required; there is no fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_longlong
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, vp, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_naive_workspace_size.argtypes = [i, i, i, i]
+    lib.attn_naive_workspace_size.restype = sz
+    lib.attn_naive_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, sz, vp]
+    lib.attn_naive_fwd.restype = i
+    lib.attn_deviation_workspace_size.argtypes = [ll]
+    lib.attn_deviation_workspace_size.restype = sz
+    lib.attn_deviation.argtypes = [vp, i, vp, i, ll, vp, sz, vp, ctypes.POINTER(DevT)]
+    lib.attn_deviation.restype = i
+    lib.attn_status.argtypes = [vp]
+    lib.attn_status.restype = i
+    lib.attn_strerror.argtypes = [i]
+    lib.attn_strerror.restype = ctypes.c_char_p
+    lib.attn_last_variant.argtypes = [ctypes.c_char_p, i]
+    lib.attn_last_variant.restype = i
+    lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint, vp]
+    lib.attn_debug_wait_timeout.restype = i
+    return lib
+
+
+lib = _load()
+
+
+def strerror(status: int) -> str:
+    return lib.attn_strerror(int(status)).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != ATTN_OK:
+        raise AttnError(rc, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _shape4(q):
+    if q.dim() == 4:
+        return q.shape
+    if q.dim() == 3:
+        return (1,) + tuple(q.shape)
+    raise ValueError("q, k, v must be [B, H, N, d] or [H, N, d]")
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, Br: int = 0, Bc: int = 0,
+             key_mask=None, out=None, lse=None, stream=None, want_lse: bool = True):
+    """Tiled exact attention forward.  Returns (o, lse).
+
+    Device tensors: the call is enqueued on `stream` (default: torch's current
+    stream) and returns immediately.  Host tensors (pinned or not): inputs are
+    copied to the current device, the kernel runs, and o / lse come back as
+    host tensors (end-to-end path).
+    """
+    if q.device.type == "cpu":
+        # End-to-end path from host memory, on torch's current stream.
+        dev = torch.device("cuda", torch.cuda.current_device())
+        qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
+        md = key_mask.to(dev, non_blocking=True) if key_mask is not None else None
+        o, l = attn_fwd(qd, kd, vd, causal, scale, Br, Bc, md, want_lse=want_lse)
+        ho = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        ho.copy_(o, non_blocking=True)
+        hl = None
+        if l is not None:
+            hl = lse if lse is not None else torch.empty(l.shape, dtype=l.dtype, pin_memory=True)
+            hl.copy_(l, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return ho, hl
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous tensors on one device")
+    if not (q.shape == k.shape == v.shape and q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share shape and dtype")
+    B, H, N, d = _shape4(q)
+    if q.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = out if out is not None else torch.empty_like(q)
+    l = lse if lse is not None else (torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+                                     if want_lse else None)
+    m = None
+    if key_mask is not None:
+        m = key_mask
+        if m.dtype != torch.float32 or not m.is_contiguous() or m.numel() != B * H * N or not m.is_cuda:
+            raise ValueError("key_mask must be a contiguous float32 device tensor with B*H*N elements")
+    rc = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, int(bool(causal)),
+                      float(scale), int(Br), int(Bc), _DTYPE[q.dtype], _ptr(m), ctypes.c_void_p(_stream(stream)))
+    _check(rc, "attn_fwd")
+    return o, l
+
+
+def attn_naive_workspace_size(B: int, H: int, N: int, dtype) -> int:
+    return int(lib.attn_naive_workspace_size(B, H, N, _DTYPE[dtype] if not isinstance(dtype, int) else dtype))
+
+
+def attn_naive_fwd(q, k, v, causal: bool = False, scale: float | None = None, key_mask=None, workspace=None,
+                   stream=None):
+    """Materialising baseline.  Returns (o, lse).  Allocates its workspace
+    with torch unless one is passed (uint8 device tensor)."""
+    B, H, N, d = _shape4(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_naive_workspace_size(B, H, N, q.dtype)
+    ws = workspace if workspace is not None else torch.empty(need, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = lib.attn_naive_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, int(bool(causal)),
+                            float(scale), _DTYPE[q.dtype], _ptr(key_mask), _ptr(ws), ws.numel(),
+                            ctypes.c_void_p(_stream(stream)))
+    _check(rc, "attn_naive_fwd")
+    return o, l
+
+
+def attn_deviation_workspace_size(n: int) -> int:
+    return int(lib.attn_deviation_workspace_size(int(n)))
+
+
+def attn_deviation(a, b, workspace=None, stream=None) -> dict:
+    """Deviation between two device tensors of equal size (synchronous)."""
+    if a.numel() != b.numel():
+        raise ValueError("a and b must have the same number of elements")
+    a = a.contiguous()
+    b = b.contiguous()
+    n = a.numel()
+    ws = workspace if workspace is not None else torch.empty(attn_deviation_workspace_size(n), dtype=torch.uint8,
+                                                             device=a.device)
+    res = DevT()
+    rc = lib.attn_deviation(_ptr(a), _DTYPE[a.dtype], _ptr(b), _DTYPE[b.dtype], n, _ptr(ws), ws.numel(),
+                            ctypes.c_void_p(_stream(stream)), ctypes.byref(res))
+    _check(rc, "attn_deviation")
+    return {"max_abs": res.max_abs, "w1": res.w1, "mean_abs": res.mean_abs, "std_abs": res.std_abs,
+            "mean_signed": res.mean_signed, "n": res.n}
+
+
+def attn_status(stream=None) -> int:
+    return int(lib.attn_status(ctypes.c_void_p(_stream(stream))))
+
+
+def attn_last_variant() -> str:
+    buf = ctypes.create_string_buffer(128)
+    lib.attn_last_variant(buf, 128)
+    return buf.value.decode()
+
+
+def attn_debug_wait_timeout(timeout_us: int, stream=None) -> int:
+    return int(lib.attn_debug_wait_timeout(int(timeout_us), ctypes.c_void_p(_stream(stream))))

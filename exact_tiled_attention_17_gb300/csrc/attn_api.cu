@@ -1,0 +1,221 @@
+// C-ABI layer: argument validation, dispatch to the kernels, the device error
+// word, status and error strings.  Declared in include/attn.h.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace eta {
+
+// One word per device that loads the library: kernels OR a code into it when
+// a bounded wait gives up.
+__device__ int g_error_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_err_ptr[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+thread_local const char *t_last_variant = "";
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(const void *Q, const void *K, const void *V, void *O, int B, int H, int N, int d, float scale,
+                 const float *key_mask) {
+    if (!Q || !K || !V || !O) return kErrArg;
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return kErrArg;
+    if (static_cast<long long>(B) * H * N >= (1LL << 31)) return kErrArg;
+    if (static_cast<long long>(N) * d >= (1LL << 31)) return kErrArg;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return kErrArg;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return kErrArg;
+    if (key_mask && (reinterpret_cast<uintptr_t>(key_mask) & 3u)) return kErrArg;
+    return kOk;
+}
+}  // namespace
+
+EncodeTiledFn encode_tiled_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode_tried) {
+        g_encode_tried = true;
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+int *device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+// Waits on a barrier that nothing completes, for timeout_us microseconds.
+__global__ void wait_timeout_probe_kernel(unsigned long long limit_ns, int *err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0u;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // Phase 0 never completes: no thread arrives.
+    mbar_wait(smem_u32(&bar), 0, &abort_flag, err, 99, limit_ns);
+    __syncthreads();
+}
+
+int launch_wait_timeout_probe(unsigned timeout_us, cudaStream_t stream) {
+    int *err = device_error_word();
+    if (!err) return kErrCuda;
+    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(timeout_us) * 1000ull, err);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+}
+
+}  // namespace eta
+
+using namespace eta;
+
+extern "C" {
+
+int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N, int d,
+             int causal, float scale, int Br, int Bc, int dtype, const float *key_mask, void *stream) {
+    int rc = check_common(Q, K, V, O, B, H, N, d, scale, key_mask);
+    if (rc != kOk) return rc;
+    if (causal != 0 && causal != 1) return kErrArg;
+    if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return kErrArg;
+    const char *variant = "";
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == ATTN_BF16) {
+        if (d != 64 && d != 128) return kErrUnsupported;
+        if (!((Br == 0 && Bc == 0) || ((Br == 64 || Br == 128) && (Bc == 64 || Bc == 128 || Bc == 256))))
+            return kErrUnsupported;
+        int dev = 0, major = 0, minor = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return kErrCuda;
+        if (major != 10 || minor != 3) return kErrUnsupported;  // built for sm_103a only
+        rc = launch_fwd_tc_bf16(Q, K, V, O, LSE, B, H, N, d, causal, scale, Br, Bc, key_mask, st, &variant);
+    } else if (dtype == ATTN_F32) {
+        if (d > 128) return kErrUnsupported;
+        if (!((Br == 0 || Br == 64) && (Bc == 0 || Bc == 64))) return kErrUnsupported;
+        rc = launch_fwd_f32(static_cast<const float *>(Q), static_cast<const float *>(K),
+                            static_cast<const float *>(V), static_cast<float *>(O), LSE, B, H, N, d, causal,
+                            scale, key_mask, st, &variant);
+    } else if (dtype == ATTN_F64) {
+        return kErrUnsupported;
+    } else {
+        return kErrArg;
+    }
+    if (rc == kOk) t_last_variant = variant;
+    return rc;
+}
+
+size_t attn_naive_workspace_size(int B, int H, int N, int dtype) {
+    if (B <= 0 || H <= 0 || N <= 0) return 0;
+    size_t es = dtype == ATTN_F32 ? 4 : dtype == ATTN_BF16 ? 2 : 0;
+    if (!es) return 0;
+    const unsigned long long rows = static_cast<unsigned long long>(B) * H * N;
+    const unsigned long long n = static_cast<unsigned long long>(N);
+    if (rows > (~0ull) / n / es) return 0;
+    return static_cast<size_t>(rows * n * es);
+}
+
+int attn_naive_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N, int d,
+                   int causal, float scale, int dtype, const float *key_mask, void *workspace, size_t ws_bytes,
+                   void *stream) {
+    int rc = check_common(Q, K, V, O, B, H, N, d, scale, key_mask);
+    if (rc != kOk) return rc;
+    if (causal != 0 && causal != 1) return kErrArg;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return dtype == ATTN_F64 ? kErrUnsupported : kErrArg;
+    if (d > 128) return kErrUnsupported;
+    const size_t need = attn_naive_workspace_size(B, H, N, dtype);
+    if (need == 0) return kErrArg;
+    if (!workspace || ws_bytes < need || !aligned16(workspace)) return kErrWorkspace;
+    return launch_naive(Q, K, V, O, LSE, B, H, N, d, causal, scale, dtype == ATTN_BF16 ? 1 : 0, key_mask,
+                        workspace, static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_deviation_workspace_size(long long n) {
+    if (n <= 0) return 0;
+    return deviation_workspace_bytes(n);
+}
+
+int attn_deviation(const void *a, int ta, const void *b, int tb, long long n, void *workspace, size_t ws_bytes,
+                   void *stream, attn_dev_t *out) {
+    if (!a || !b || !out || n <= 0) return kErrArg;
+    if (ta < ATTN_F32 || ta > ATTN_F64 || tb < ATTN_F32 || tb > ATTN_F64) return kErrArg;
+    const size_t need = deviation_workspace_bytes(n);
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return kErrWorkspace;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    double *res = reinterpret_cast<double *>(static_cast<char *>(workspace) + deviation_result_offset(n));
+    int rc = launch_deviation(a, ta, b, tb, n, workspace, st, res);
+    if (rc != kOk) return rc;
+    double host[5];
+    if (cudaMemcpyAsync(host, res, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess) return kErrCuda;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return kErrCuda;
+    out->max_abs = host[0];
+    out->w1 = host[1];
+    out->mean_abs = host[2];
+    out->std_abs = host[3];
+    out->mean_signed = host[4];
+    out->n = n;
+    return kOk;
+}
+
+int attn_status(void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return kErrCuda;
+    int *err = device_error_word();
+    if (!err) return kErrCuda;
+    int host = 0;
+    if (cudaMemcpy(&host, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return kErrCuda;
+    if (host != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return kErrCuda;
+        return kErrDeviceTimeout;
+    }
+    return kOk;
+}
+
+const char *attn_strerror(int status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case ATTN_ERR_CUDA: return "CUDA runtime or driver error";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int attn_last_variant(char *buf, int len) {
+    if (!buf || len <= 0) return kErrArg;
+    const int n = static_cast<int>(strlen(t_last_variant));
+    snprintf(buf, static_cast<size_t>(len), "%s", t_last_variant);
+    return n;
+}
+
+int attn_debug_wait_timeout(unsigned timeout_us, void *stream) {
+    if (timeout_us < 1 || timeout_us > 1000000u) return kErrArg;
+    return launch_wait_timeout_probe(timeout_us, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,539 @@
+// Exact tiled attention forward, bf16 in / f32 accumulate, for sm_103a.
+//
+// What it computes: O = softmax(Q K^T * scale + mask) V and the per-row
+// natural-log LSE ("Is Flash Attention Stable?" §II-A), tile by tile as in
+// its §II-B / Fig. 1, never forming the N x N score matrix.  Each query row
+// carries the online-softmax state of the yadro-code.ru FlashAttention
+// tutorial: a running maximum m, a running denominator l and an
+// unnormalised accumulator that is multiplied by exp(m_old - m_new) when the
+// maximum grows, with one division at the end.
+//
+// GB300 mapping (one CTA per group of NQ consecutive 128-row query tiles of
+// one (batch, head)):
+//   warp 4*NQ      TMA producer: Q tiles once, then K_j / V_j tiles into a
+//                  ring of NS shared-memory slots (128-byte swizzle).
+//   warp 4*NQ + 1  MMA issuer (one thread): S_q = Q_q K_j^T and
+//                  O_q += P_q V_j on tcgen05, accumulators in tensor memory.
+//   warps 4q..4q+3 softmax warpgroup of query tile q: one thread per row
+//                  (TMEM lane = row).  Reads S_q, applies scale and masks,
+//                  updates (m, l), rescales O_q in TMEM when needed, writes
+//                  P_q as bf16 back over S_q's columns (the A operand of the
+//                  next MMA comes straight from TMEM), then the epilogue.
+// The MMA issue order S_0(j+1) after PV_0(j), S_1(j+1) after PV_1(j) lets the
+// tensor pipe work on one tile while the other tile's softmax runs.
+//
+// The reference maximum is moved only when the tile maximum exceeds it by
+// more than kRescaleThresh (log2 units): exact up to rounding because a / l
+// does not depend on the reference point, and p = 2^(x - m) stays <= 2^8.
+// The denominator l sums the same bf16-rounded p that enter P V, so the
+// normalised weights are the ones actually applied.
+#include <cuda_bf16.h>
+#include <cstdio>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace eta {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThresh = 8.0f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+template <int D, int BC, int NQ>
+struct TcShape {
+    static constexpr int BR = 128;
+    static constexpr int CB = D / 64;               // 128-byte column blocks per row
+    static constexpr int Q_BYTES = BR * D * 2;      // one Q (or O staging) tile
+    static constexpr int SLOT_BYTES = BC * D * 2;   // one K or V tile
+    static constexpr int SMEM_BUDGET = 200 * 1024;
+    static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES) / SLOT_BYTES;
+    static constexpr int NS = NS_RAW > 8 ? 8 : (NS_RAW < 2 ? 2 : NS_RAW);
+    static constexpr int TMEM_USED = NQ * (BC + D);
+    static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32
+                                     : TMEM_USED <= 64 ? 64
+                                     : TMEM_USED <= 128 ? 128
+                                     : TMEM_USED <= 256 ? 256 : 512;
+    static constexpr int SOFTMAX_WARPS = 4 * NQ;
+    static constexpr int WARP_TMA = SOFTMAX_WARPS;
+    static constexpr int WARP_MMA = SOFTMAX_WARPS + 1;
+    static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+    // shared memory layout (offsets from a 1024-byte aligned base)
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_RING = NQ * Q_BYTES;
+    static constexpr int OFF_BAR = OFF_RING + NS * SLOT_BYTES;
+    // barriers: q_full[NQ] full[NS] empty[NS] s_full[NQ] p_full[NQ] o_full[NQ] done
+    static constexpr int BAR_QFULL = 0;
+    static constexpr int BAR_FULL = BAR_QFULL + NQ;
+    static constexpr int BAR_EMPTY = BAR_FULL + NS;
+    static constexpr int BAR_SFULL = BAR_EMPTY + NS;
+    static constexpr int BAR_PFULL = BAR_SFULL + NQ;
+    static constexpr int BAR_OFULL = BAR_PFULL + NQ;
+    static constexpr int BAR_DONE = BAR_OFULL + NQ;
+    static constexpr int NBARS = BAR_DONE + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+
+    __host__ __device__ static constexpr int s_col(int q) { return q * BC; }
+    __host__ __device__ static constexpr int o_col(int q) { return NQ * BC + q * D; }
+
+    static_assert(D == 64 || D == 128, "head dim");
+    static_assert(BC == 64 || BC == 128 || BC == 256, "key tile");
+    static_assert(TMEM_USED <= 512, "tensor memory budget");
+    // A 512-column allocation must never wait for another resident CTA.
+    static_assert(TMEM_COLS < 512 || SMEM_BYTES > 116 * 1024, "one CTA per SM for full TMEM");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+struct TcParams {
+    int N;              // sequence length
+    int BH;             // B * H
+    int num_qg;         // query groups (NQ * 128 rows) per head
+    int causal;
+    float scale_log2;   // scale * log2(e)
+    const float *key_mask;  // [BH][N] additive, or null
+    float *lse;             // [BH][N], or null
+    int *err;               // device error word
+};
+
+template <int D, int BC, int NQ, bool MASKED>
+__global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                       const TcParams p) {
+    using S = TcShape<D, BC, NQ>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- work item: heaviest query groups (largest rows) launch first ----
+    const int lin = blockIdx.x;
+    const int qg = p.num_qg - 1 - lin / p.BH;
+    const int bh = lin % p.BH;
+    const int N = p.N;
+    const int nkv_all = (N + BC - 1) / BC;
+    int r0[NQ], nkv[NQ];
+    int nkv_max = 0;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        r0[q] = (qg * NQ + q) * 128;
+        if (r0[q] >= N) {
+            nkv[q] = 0;
+        } else if (p.causal) {
+            const int last_row = min(r0[q] + 127, N - 1);
+            nkv[q] = min(nkv_all, last_row / BC + 1);
+        } else {
+            nkv[q] = nkv_all;
+        }
+        nkv_max = max(nkv_max, nkv[q]);
+    }
+
+    auto bar = [&](int i) -> uint32_t { return sbase + S::OFF_BAR + 8 * i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::OFF_MISC);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + S::OFF_MISC + 4);
+    const uint32_t sQ = sbase + S::OFF_Q;
+    const uint32_t sRing = sbase + S::OFF_RING;
+
+    if (threadIdx.x == 0) {
+        for (int q = 0; q < NQ; ++q) {
+            mbar_init(bar(S::BAR_QFULL + q), 1);
+            mbar_init(bar(S::BAR_SFULL + q), 1);
+            mbar_init(bar(S::BAR_PFULL + q), 128);
+            mbar_init(bar(S::BAR_OFULL + q), 1);
+        }
+        for (int s = 0; s < S::NS; ++s) {
+            mbar_init(bar(S::BAR_FULL + s), 1);
+            mbar_init(bar(S::BAR_EMPTY + s), 1);
+        }
+        mbar_init(bar(S::BAR_DONE), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == S::WARP_MMA) {
+        tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == S::WARP_TMA) {
+        // ------------------------------------------------------------------
+        // TMA producer
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_o);
+            const uint64_t pol_kv = l2_policy_evict_last();   // K/V are re-read by every query group
+            const uint64_t pol_q = l2_policy_evict_first();   // Q is read once
+            for (int q = 0; q < NQ; ++q) {
+                if (nkv[q] == 0) continue;
+                mbar_arrive_expect_tx(bar(S::BAR_QFULL + q), S::Q_BYTES);
+#pragma unroll
+                for (int cb = 0; cb < S::CB; ++cb)
+                    tma_load_3d_hint(sQ + q * S::Q_BYTES + cb * (128 * 128), &tm_q, bar(S::BAR_QFULL + q),
+                                     cb * 64, r0[q], bh, pol_q);
+            }
+            const int T = 2 * nkv_max;  // K_0 V_0 K_1 V_1 ...
+            int issued = 0;
+            for (int t = 0; t < T; ++t) {
+                const int slot = t % S::NS, round = t / S::NS;
+                if (round > 0 &&
+                    !mbar_wait(bar(S::BAR_EMPTY + slot), (round - 1) & 1, abort_flag, p.err, 1))
+                    break;
+                mbar_arrive_expect_tx(bar(S::BAR_FULL + slot), S::SLOT_BYTES);
+                const CUtensorMap *m = (t & 1) ? &tm_v : &tm_k;
+                const int j = t >> 1;
+#pragma unroll
+                for (int cb = 0; cb < S::CB; ++cb)
+                    tma_load_3d_hint(sRing + slot * S::SLOT_BYTES + cb * (BC * 128), m, bar(S::BAR_FULL + slot),
+                                     cb * 64, j * BC, bh, pol_kv);
+                issued = t + 1;
+            }
+            // Drain: every copy this thread started has landed before the CTA
+            // may exit (normally already true).
+            for (int t = max(0, issued - S::NS); t < issued; ++t)
+                mbar_wait(bar(S::BAR_FULL + t % S::NS), (t / S::NS) & 1, abort_flag, p.err, 2);
+            for (int q = 0; q < NQ; ++q)
+                if (nkv[q] > 0) mbar_wait(bar(S::BAR_QFULL + q), 0, abort_flag, p.err, 3);
+        }
+        __syncwarp();
+    } else if (warp == S::WARP_MMA) {
+        // ------------------------------------------------------------------
+        // MMA issuer (one thread)
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(128, BC, false, false);  // Q, K both K-major
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);    // P (TMEM), V MN-major
+            bool ok = true;
+            for (int q = 0; q < NQ && ok; ++q)
+                if (nkv[q] > 0) ok = mbar_wait(bar(S::BAR_QFULL + q), 0, abort_flag, p.err, 10);
+
+            auto issue_s = [&](int q, int j) {
+                const uint32_t kslot = sRing + ((2 * j) % S::NS) * S::SLOT_BYTES;
+                const uint32_t qbuf = sQ + q * S::Q_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int cb = kk >> 2, off = (kk & 3) * 32;
+                    const uint64_t a = sdesc_sw128(qbuf + cb * (128 * 128) + off, 16, 1024);
+                    const uint64_t b = sdesc_sw128(kslot + cb * (BC * 128) + off, 16, 1024);
+                    mma_bf16_ss(tmem + S::s_col(q), a, b, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(S::BAR_SFULL + q));
+            };
+            auto issue_pv = [&](int q, int j) {
+                const uint32_t vslot = sRing + ((2 * j + 1) % S::NS) * S::SLOT_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BC / 16; ++kk) {
+                    const uint64_t b = sdesc_sw128(vslot + kk * 2048, BC * 128, 1024);
+                    mma_bf16_ts(tmem + S::o_col(q), tmem + S::s_col(q) + kk * 8, b, idesc_o,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+
+            if (ok && nkv_max > 0) {
+                ok = mbar_wait(bar(S::BAR_FULL + 0), 0, abort_flag, p.err, 11);  // K_0
+                if (ok) {
+                    tc_fence_after();
+                    for (int q = 0; q < NQ; ++q)
+                        if (nkv[q] > 0) issue_s(q, 0);
+                    tc_commit(bar(S::BAR_EMPTY + 0));
+                }
+            }
+            for (int j = 0; ok && j < nkv_max; ++j) {
+                const int tv = 2 * j + 1;
+                if (!mbar_wait(bar(S::BAR_FULL + tv % S::NS), (tv / S::NS) & 1, abort_flag, p.err, 12)) break;
+                tc_fence_after();
+                bool k_ready = false;
+                const int tk = 2 * j + 2;
+                for (int q = 0; q < NQ && ok; ++q) {
+                    if (j >= nkv[q]) continue;
+                    if (!mbar_wait(bar(S::BAR_PFULL + q), j & 1, abort_flag, p.err, 13)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(q, j);
+                    if (j == nkv[q] - 1) tc_commit(bar(S::BAR_OFULL + q));
+                    if (j + 1 < nkv[q]) {
+                        if (!k_ready) {
+                            if (!mbar_wait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, abort_flag, p.err, 14)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            k_ready = true;
+                        }
+                        issue_s(q, j + 1);
+                    }
+                }
+                tc_commit(bar(S::BAR_EMPTY + tv % S::NS));            // V_j slot
+                if (k_ready) tc_commit(bar(S::BAR_EMPTY + tk % S::NS));  // K_{j+1} slot
+            }
+            // Every MMA issued has completed before tensor memory is released.
+            tc_commit(bar(S::BAR_DONE));
+            mbar_wait(bar(S::BAR_DONE), 0, abort_flag, p.err, 15);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------
+        // Softmax warpgroup of query tile q
+        // ------------------------------------------------------------------
+        const int q = warp >> 2;
+        const int wq = warp & 3;
+        const int row_in = wq * 32 + lane;
+        const int row = r0[q] + row_in;
+        const uint32_t t_lane = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + t_lane + S::s_col(q);
+        const uint32_t tO = tmem + t_lane + S::o_col(q);
+        const float sl2 = p.scale_log2;
+        const float *mrow = MASKED ? p.key_mask + static_cast<size_t>(bh) * N : nullptr;
+        float m = kNegInf;  // reference maximum, log2 units
+        float l = 0.f;
+        bool ok = true;
+
+        for (int j = 0; j < nkv[q]; ++j) {
+            if (!mbar_wait(bar(S::BAR_SFULL + q), j & 1, abort_flag, p.err, 20)) { ok = false; break; }
+            tc_fence_after();
+            const int key0 = j * BC;
+            // Tiles that need per-element masking: the N tail, the causal
+            // diagonal, or any tile when a key mask is given.
+            const bool edge = MASKED || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0[q]);
+
+            // Transform one loaded 32-column chunk into log2-domain scores
+            // x = s*scale*log2(e) (+ mask*log2(e)), -inf where not allowed.
+            auto mask_chunk = [&](int c, uint32_t *r) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int key = key0 + 32 * c + e;
+                    float x = __uint_as_float(r[e]) * sl2;
+                    if (MASKED) x = (key < N) ? fmaf(__ldg(mrow + key), kLog2e, x) : kNegInf;
+                    const bool allowed = (key < N) && (!p.causal || key <= row);
+                    r[e] = __float_as_uint(allowed ? x : kNegInf);
+                }
+            };
+            // p = 2^(x - m_use) for one chunk, packed to bf16 pairs and written
+            // over S's first BC/2 columns (chunk c -> columns 16c .. 16c+15,
+            // never ahead of the chunks still to be read).
+            auto exp_chunk = [&](int c, const uint32_t *r, float m_use, float &rs) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float x0 = __uint_as_float(r[2 * e]);
+                    const float x1 = __uint_as_float(r[2 * e + 1]);
+                    const float p0 = edge ? ex2(x0 - m_use) : ex2(fmaf(x0, sl2, -m_use));
+                    const float p1 = edge ? ex2(x1 - m_use) : ex2(fmaf(x1, sl2, -m_use));
+                    pk[e] = pack_bf16x2(p0, p1);
+                    rs += bf16lo_to_f32(pk[e]) + bf16hi_to_f32(pk[e]);
+                }
+                tmem_st16(tS + 16 * c, pk);
+            };
+            auto chunk_max = [&](const uint32_t *r, float mx) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
+                return mx;
+            };
+
+            constexpr bool kTwoPass = BC > 128;   // 256 columns do not fit in registers
+            constexpr int kRegCols = kTwoPass ? 32 : BC;
+            uint32_t sr[kRegCols];
+            float mx = kNegInf;
+            if constexpr (!kTwoPass) {
+#pragma unroll
+                for (int c = 0; c < BC / 32; ++c) tmem_ld32(tS + 32 * c, sr + 32 * c);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < BC / 32; ++c) reg_fence32(sr + 32 * c);
+                if (edge) {
+#pragma unroll
+                    for (int c = 0; c < BC / 32; ++c) {
+                        mask_chunk(c, sr + 32 * c);
+                        mx = chunk_max(sr + 32 * c, mx);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BC / 32; ++c) mx = chunk_max(sr + 32 * c, mx);
+                    mx *= sl2;   // scale > 0: max commutes with the scaling
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BC / 32; ++c) {
+                    tmem_ld32(tS + 32 * c, sr);
+                    tmem_ld_wait();
+                    reg_fence32(sr);
+                    if (edge) mask_chunk(c, sr);
+                    mx = chunk_max(sr, mx);
+                }
+                if (!edge) mx *= sl2;
+            }
+
+            const float m_new = (mx > m + kRescaleThresh) ? mx : m;
+            const bool moved = (m_new != m);
+            const float alpha = moved ? ex2(m - m_new) : 1.f;
+            const float m_use = (m_new == kNegInf) ? 0.f : m_new;
+            if (j > 0 && __any_sync(0xffffffffu, moved)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32 * c, o);
+                    tmem_ld_wait();
+                    reg_fence32(o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tO + 32 * c, o);
+                }
+            }
+            m = m_new;
+
+            float rs = 0.f;
+            if constexpr (!kTwoPass) {
+#pragma unroll
+                for (int c = 0; c < BC / 32; ++c) exp_chunk(c, sr + 32 * c, m_use, rs);
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BC / 32; ++c) {
+                    tmem_ld32(tS + 32 * c, sr);
+                    tmem_ld_wait();
+                    reg_fence32(sr);
+                    if (edge) mask_chunk(c, sr);
+                    exp_chunk(c, sr, m_use, rs);
+                }
+            }
+            l = l * alpha + rs;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(S::BAR_PFULL + q));
+        }
+
+        // ---------------- epilogue ----------------
+        if (nkv[q] > 0) {
+            if (ok) ok = mbar_wait(bar(S::BAR_OFULL + q), 0, abort_flag, p.err, 21);
+            tc_fence_after();
+            const float inv = (l > 0.f) ? 1.f / l : 0.f;
+            const uint32_t stage = sQ + q * S::Q_BYTES;  // Q_q is no longer read
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32 * c, o);
+                tmem_ld_wait();
+                reg_fence32(o);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                const int cb = c >> 1;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int ch = (c & 1) * 4 + k;  // 16-byte chunk within the 128-byte row
+                    const uint32_t addr = stage + cb * (128 * 128) + row_in * 128 + ((ch ^ (row_in & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * k]),
+                                 "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
+                                 : "memory");
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1 + q, 128);
+            if (row_in == 0 && !*abort_flag) {
+#pragma unroll
+                for (int cb = 0; cb < S::CB; ++cb)
+                    tma_store_3d(&tm_o, stage + cb * (128 * 128), cb * 64, r0[q], bh);
+                tma_store_commit();
+                tma_store_wait_read0();
+            }
+            if (p.lse != nullptr && row < N) {
+                p.lse[static_cast<size_t>(bh) * N + row] =
+                    (l > 0.f) ? (m + log2f(l)) * kLn2 : kNegInf;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == S::WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, S::TMEM_COLS);
+    }
+}
+
+bool make_map(CUtensorMap *m, const void *base, int D, int N, int BH, int box_rows) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int BC, int NQ, bool MASKED>
+int launch_variant(const void *Q, const void *K, const void *V, void *O, float *LSE, int BH, int N,
+                   int causal, float scale, const float *key_mask, cudaStream_t stream) {
+    using S = TcShape<D, BC, NQ>;
+    auto kern = attn_fwd_tc_kernel<D, BC, NQ, MASKED>;
+    static int attr_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
+    if (attr_device != dev) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES) != cudaSuccess)
+            return kErrCuda;
+        attr_device = dev;
+    }
+    CUtensorMap tq, tk, tv, to;
+    if (!make_map(&tq, Q, D, N, BH, 128) || !make_map(&tk, K, D, N, BH, BC) || !make_map(&tv, V, D, N, BH, BC) ||
+        !make_map(&to, O, D, N, BH, 128))
+        return kErrCuda;
+    TcParams p;
+    p.N = N;
+    p.BH = BH;
+    p.num_qg = (N + NQ * 128 - 1) / (NQ * 128);
+    p.causal = causal;
+    p.scale_log2 = scale * kLog2e;
+    p.key_mask = key_mask;
+    p.lse = LSE;
+    p.err = device_error_word();
+    if (!p.err) return kErrCuda;
+    const long long grid = static_cast<long long>(p.num_qg) * BH;
+    if (grid > 0x7fffffffLL) return kErrUnsupported;
+    kern<<<static_cast<unsigned>(grid), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+}
+
+template <int D, int BC>
+int launch_dbc(const void *Q, const void *K, const void *V, void *O, float *LSE, int BH, int N, int causal,
+               float scale, const float *key_mask, cudaStream_t stream, const char **variant) {
+    constexpr int NQ = (2 * (BC + D) <= 512) ? 2 : 1;
+    static char name[64];
+    snprintf(name, sizeof(name), "tc_bf16_d%d_br128_bc%d_nq%d%s", D, BC, NQ, key_mask ? "_mask" : "");
+    if (variant) *variant = name;
+    if (key_mask)
+        return launch_variant<D, BC, NQ, true>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream);
+    return launch_variant<D, BC, NQ, false>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream);
+}
+
+}  // namespace
+
+int launch_fwd_tc_bf16(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
+                       int d, int causal, float scale, int Br, int Bc, const float *key_mask,
+                       cudaStream_t stream, const char **variant) {
+    if (Br == 0 && Bc == 0) { Br = 128; Bc = 128; }
+    if (Br != 128) return kErrUnsupported;
+    const int BH = B * H;
+    if (d == 64) {
+        if (Bc == 64) return launch_dbc<64, 64>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+        if (Bc == 128) return launch_dbc<64, 128>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+        if (Bc == 256) return launch_dbc<64, 256>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+    } else if (d == 128) {
+        if (Bc == 64) return launch_dbc<128, 64>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+        if (Bc == 128) return launch_dbc<128, 128>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+        if (Bc == 256) return launch_dbc<128, 256>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+    }
+    return kErrUnsupported;
+}
+
+}  // namespace eta

@@ -1,0 +1,53 @@
+// Internal interfaces between the C-ABI layer (attn_api.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace eta {
+
+// Status codes (mirror attn_status_t in include/attn.h).
+constexpr int kOk = 0;
+constexpr int kErrArg = -1;
+constexpr int kErrUnsupported = -2;
+constexpr int kErrWorkspace = -3;
+constexpr int kErrCuda = -4;
+constexpr int kErrDeviceTimeout = -5;
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// Device address of the library's error word on the current device (or null).
+int *device_error_word();
+
+// BF16 tiled forward on tcgen05 (fwd_tc.cu).  variant receives a static name.
+int launch_fwd_tc_bf16(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                       int N, int d, int causal, float scale, int Br, int Bc, const float *key_mask,
+                       cudaStream_t stream, const char **variant);
+
+// FP32 tiled forward on the CUDA cores (fwd_f32.cu).
+int launch_fwd_f32(const float *Q, const float *K, const float *V, float *O, float *LSE, int B, int H,
+                   int N, int d, int causal, float scale, const float *key_mask, cudaStream_t stream,
+                   const char **variant);
+
+// Materialising baseline (naive.cu).  dtype: 0 f32, 1 bf16.
+int launch_naive(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
+                 int d, int causal, float scale, int dtype, const float *key_mask, void *workspace,
+                 cudaStream_t stream);
+
+// Deviation measures (deviation.cu).
+size_t deviation_workspace_bytes(long long n);
+int launch_deviation(const void *a, int ta, const void *b, int tb, long long n, void *workspace,
+                     cudaStream_t stream, double *dev_result /* 5 doubles inside workspace */);
+size_t deviation_result_offset(long long n);
+
+// Bounded-wait self-test kernel (attn_api.cu).
+int launch_wait_timeout_probe(unsigned timeout_us, cudaStream_t stream);
+
+}  // namespace eta

@@ -1,0 +1,167 @@
+/*
+ * Exact tiled attention forward on one NVIDIA GB300 (sm_103a): C ABI.
+ *
+ * Library: exact_tiled_attention_17_gb300/libattn.so.  Every entry point has
+ * C linkage and takes plain pointers and sizes.  No entry point allocates
+ * device memory: tensors and workspaces are owned by the caller.  Work is
+ * enqueued on the caller's stream (a cudaStream_t passed as void*; NULL means
+ * the legacy default stream) on the current device.
+ *
+ * Errors are reported synchronously through the return value and nothing is
+ * launched when an argument is rejected.  There is no CPU fallback and no
+ * other backend: a missing GPU or an unsupported device returns
+ * ATTN_ERR_CUDA / ATTN_ERR_UNSUPPORTED.  Errors found while a kernel runs
+ * (a bounded wait that ran out) are recorded in a device-side error word that
+ * attn_status() reads.
+ *
+ * The computation is the attention of "Is Flash Attention Stable?" §II-A,
+ *     O = softmax(Q K^T * scale + mask) V,
+ * evaluated as in its §II-B (Fig. 1): tile by tile, without materialising the
+ * N x N score matrix, with the online-softmax rescale of the yadro-code.ru
+ * FlashAttention tutorial (running row maximum m, running denominator l,
+ * unnormalised accumulator multiplied by exp(m_old - m_new) when the maximum
+ * grows, one division at the end).
+ *
+ * Common conventions
+ *   Q, K, V, O   [B][H][N][d] row-major, contiguous, device memory, base
+ *                pointers 16-byte aligned.  O has the dtype of Q/K/V.
+ *   LSE          [B][H][N] float32, device memory, natural-log log-sum-exp of
+ *                each row's scaled and masked scores; may be NULL (not written).
+ *   causal       0 or 1.  Top-left aligned: query i sees keys j <= i (the
+ *                tutorial's causal prefixes).
+ *   scale        multiplies Q K^T; callers normally pass 1/sqrt(d).  Must be
+ *                finite and > 0.
+ *   key_mask     NULL, or [B][H][N] float32 device memory added to every row's
+ *                score of key j (a key-padding mask).  Entries must be finite
+ *                or -inf; -inf removes the key.  There is no finite "masked"
+ *                sentinel anywhere in the library: the aicompass.dev note on
+ *                FlashInfer kernels shows why a hard-coded -50,000 is wrong.
+ *   A row whose every score is -inf (fully masked) outputs O = 0 and
+ *   LSE = -inf, with no NaN.  (The tutorial assumes each row has an allowed
+ *   key and leaves this case to be defined; this is the definition.)
+ */
+#ifndef EXACT_TILED_ATTENTION_ATTN_H
+#define EXACT_TILED_ATTENTION_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1, ATTN_F64 = 2 } attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_ARG = -1,            /* null pointer, bad size, bad alignment, bad scale      */
+    ATTN_ERR_UNSUPPORTED = -2,    /* valid but not implemented: d, Br/Bc, dtype, device    */
+    ATTN_ERR_WORKSPACE = -3,      /* workspace NULL or smaller than the size query returns */
+    ATTN_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed                     */
+    ATTN_ERR_DEVICE_TIMEOUT = -5  /* a kernel's bounded wait ran out (see attn_status)     */
+} attn_status_t;
+
+/*
+ * attn_fwd — the tiled exact forward pass ("Is Flash Attention Stable?"
+ * §II-B and Fig. 1; the tutorial's online merge).
+ *
+ * dtype ATTN_BF16: Q/K/V/O bfloat16.  Both contractions run on the tcgen05
+ *   tensor cores with bf16 operands and float32 accumulation in tensor
+ *   memory; softmax state (m, l) and the accumulator stay float32; the
+ *   probabilities P are rounded to bf16 (round-to-nearest-even) as the
+ *   operand of the second contraction and O is rounded to bf16 at the end.
+ *   d must be 64 or 128.  Br in {64, 128}, Bc in {64, 128, 256};
+ *   Br = Bc = 0 selects (128, 128).
+ * dtype ATTN_F32: Q/K/V/O float32, every operation in float32 on the CUDA
+ *   cores (no TF32).  1 <= d <= 128.  Br and Bc must be 0 or 64.
+ * N >= 1 with any tail; B, H >= 1; B*H*N < 2^31 rows.
+ * Asynchronous: returns after enqueueing on `stream`.
+ */
+int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+             int B, int H, int N, int d, int causal, float scale, int Br, int Bc,
+             int dtype, const float *key_mask, void *stream);
+
+/*
+ * attn_naive_workspace_size — bytes of workspace attn_naive_fwd needs:
+ * B*H*N*N elements of the input dtype (the materialised score matrix; the
+ * tutorial's arithmetic: 8192 tokens x 2 bytes = 128 MiB per head, 4 GiB for
+ * 32 heads).  Returns 0 for invalid arguments or on overflow.
+ */
+size_t attn_naive_workspace_size(int B, int H, int N, int dtype);
+
+/*
+ * attn_naive_fwd — "baseline attention" (the paper's §IV comparison point):
+ * materialises S = Q K^T * scale + mask in the caller's workspace, stored in
+ * the input dtype; a row softmax with float32 arithmetic overwrites S with
+ * P, stored in the input dtype; then O = P V with float32 accumulation,
+ * stored in the input dtype.  Same masking, causal and fully-masked-row
+ * conventions as attn_fwd.  dtype ATTN_F32 or ATTN_BF16, 1 <= d <= 128.
+ * workspace: device memory of at least attn_naive_workspace_size() bytes.
+ * Asynchronous.
+ */
+int attn_naive_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                   int B, int H, int N, int d, int causal, float scale, int dtype,
+                   const float *key_mask, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Deviation between two tensors (the paper's §IV-A maximum element-wise
+ * difference and §V Wasserstein distance; the pages' own formulas were lost
+ * in extraction, these are the standard definitions):
+ *   max_abs     = max_i |a_i - b_i|
+ *   w1          = 1-D Wasserstein-1 between the empirical value distributions
+ *                 of a and b, (1/n) * sum_i |sort(a)_i - sort(b)_i|
+ *   mean_abs    = mean of |a_i - b_i|;   std_abs = its population std
+ *   mean_signed = mean of (a_i - b_i)
+ * Elements where a_i == b_i (including equal infinities) contribute 0.
+ * All arithmetic is float64; inputs are converted exactly.
+ */
+typedef struct {
+    double max_abs, w1, mean_abs, std_abs, mean_signed;
+    long long n;
+} attn_dev_t;
+
+/* Bytes of device workspace attn_deviation needs for n elements (0 if n <= 0). */
+size_t attn_deviation_workspace_size(long long n);
+
+/*
+ * attn_deviation — a (dtype ta) and b (dtype tb): n elements each, device
+ * memory, any of ATTN_F32 / ATTN_BF16 / ATTN_F64, naturally aligned.
+ * workspace: device memory of at least attn_deviation_workspace_size(n)
+ * bytes, 256-byte aligned.  Synchronous: waits for `stream` and writes the
+ * result to the host struct *out.
+ */
+int attn_deviation(const void *a, int ta, const void *b, int tb, long long n,
+                   void *workspace, size_t ws_bytes, void *stream, attn_dev_t *out);
+
+/*
+ * attn_status — waits for `stream`, then returns ATTN_ERR_DEVICE_TIMEOUT if a
+ * kernel of this library recorded a timed-out wait since the last call
+ * (and clears the record), ATTN_ERR_CUDA if the stream reports a CUDA error,
+ * else ATTN_OK.
+ */
+int attn_status(void *stream);
+
+/* attn_strerror — static text for a status code. */
+const char *attn_strerror(int status);
+
+/*
+ * attn_last_variant — writes the name of the kernel variant the last
+ * successful attn_fwd call on this thread launched (e.g.
+ * "tc_bf16_d128_br128_bc128_nq2") into buf (NUL-terminated, truncated to
+ * len).  Returns the full length, or ATTN_ERR_ARG.
+ */
+int attn_last_variant(char *buf, int len);
+
+/*
+ * attn_debug_wait_timeout — self-test of the device-side failure path: one
+ * small kernel waits on a shared-memory barrier that nothing will ever
+ * complete, gives up after `timeout_us` microseconds (1 .. 10^6), records
+ * ATTN_ERR_DEVICE_TIMEOUT in the error word and returns.  The context stays
+ * usable; the next attn_status() reports the timeout and clears it.
+ */
+int attn_debug_wait_timeout(unsigned timeout_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_TILED_ATTENTION_ATTN_H */

@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI: the library builds, loads without a GPU,
+exports every symbol include/attn.h declares, and rejects bad arguments
+synchronously without launching anything."""
+import ctypes
+import importlib.util
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    spec = importlib.util.spec_from_file_location(
+        "_eta_build", os.path.join(ROOT, "exact_tiled_attention_17_gb300", "_build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    path = mod.build()
+    return ctypes.CDLL(path)
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*(attn_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("attn_fwd", "attn_naive_fwd", "attn_deviation"):
+        assert must in names
+    assert len(names) >= 9
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_exports_match_header():
+    import exact_tiled_attention_17_gb300 as eta
+    assert sorted(eta.EXPORTS) == _declared_functions()
+
+
+def test_sizes_and_strings(lib):
+    lib.attn_naive_workspace_size.restype = ctypes.c_size_t
+    lib.attn_naive_workspace_size.argtypes = [ctypes.c_int] * 4
+    # the tutorial's arithmetic: 8192 tokens, 2-byte scores: 128 MiB per head, 4 GiB for 32 heads
+    assert lib.attn_naive_workspace_size(1, 1, 8192, 1) == 128 * 2 ** 20
+    assert lib.attn_naive_workspace_size(1, 32, 8192, 1) == 4 * 2 ** 30
+    assert lib.attn_naive_workspace_size(1, 1, 100, 0) == 100 * 100 * 4
+    assert lib.attn_naive_workspace_size(0, 1, 100, 0) == 0
+    assert lib.attn_naive_workspace_size(1, 1, 100, 7) == 0
+    lib.attn_deviation_workspace_size.restype = ctypes.c_size_t
+    lib.attn_deviation_workspace_size.argtypes = [ctypes.c_longlong]
+    assert lib.attn_deviation_workspace_size(0) == 0
+    assert lib.attn_deviation_workspace_size(1000) >= 3 * 8 * 1000
+    lib.attn_strerror.restype = ctypes.c_char_p
+    lib.attn_strerror.argtypes = [ctypes.c_int]
+    for code in range(-5, 1):
+        assert lib.attn_strerror(code)
+    assert b"timed out" in lib.attn_strerror(-5)
+
+
+def _fwd(lib, **kw):
+    args = dict(Q=16, K=16, V=16, O=16, LSE=0, B=1, H=1, N=8, d=64, causal=0, scale=0.125, Br=0, Bc=0,
+                dtype=1, mask=0, stream=0)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    f = lib.attn_fwd
+    f.restype = ctypes.c_int
+    f.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [ctypes.c_float] + [ctypes.c_int] * 3 + [vp, vp]
+    return f(vp(args["Q"]) if args["Q"] else None, vp(args["K"]) if args["K"] else None,
+             vp(args["V"]) if args["V"] else None, vp(args["O"]) if args["O"] else None,
+             vp(args["LSE"]) if args["LSE"] else None, args["B"], args["H"], args["N"], args["d"],
+             args["causal"], args["scale"], args["Br"], args["Bc"], args["dtype"],
+             vp(args["mask"]) if args["mask"] else None, None)
+
+
+def test_argument_rejection_without_launch(lib):
+    # fake, never dereferenced pointers: every call must be rejected on the host
+    assert _fwd(lib, Q=0) == -1
+    assert _fwd(lib, N=0) == -1
+    assert _fwd(lib, B=-1) == -1
+    assert _fwd(lib, scale=0.0) == -1
+    assert _fwd(lib, scale=float("nan")) == -1
+    assert _fwd(lib, scale=-1.0) == -1
+    assert _fwd(lib, Q=24) == -1                  # not 16-byte aligned
+    assert _fwd(lib, causal=2) == -1
+    assert _fwd(lib, mask=18) == -1               # mask not 4-byte aligned
+    assert _fwd(lib, dtype=9) == -1
+    assert _fwd(lib, d=96) == -2                  # bf16 supports d in {64, 128}
+    assert _fwd(lib, Br=32, Bc=64) == -2
+    assert _fwd(lib, Br=128, Bc=96) == -2
+    assert _fwd(lib, dtype=0, d=129) == -2
+    assert _fwd(lib, dtype=0, Br=128, Bc=128) == -2
+    assert _fwd(lib, dtype=2) == -2
+
+
+def test_naive_and_deviation_rejection(lib):
+    vp = ctypes.c_void_p
+    f = lib.attn_naive_fwd
+    f.restype = ctypes.c_int
+    f.argtypes = [vp] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]
+    p = vp(16)
+    assert f(p, p, p, p, None, 1, 1, 8, 64, 0, 0.125, 1, None, None, 0, None) == -3      # no workspace
+    assert f(p, p, p, p, None, 1, 1, 8, 64, 0, 0.125, 1, None, p, 100, None) == -3       # too small
+    assert f(p, p, p, p, None, 1, 1, 8, 200, 0, 0.125, 1, None, p, 1 << 20, None) == -2  # d > 128
+    g = lib.attn_deviation
+    g.restype = ctypes.c_int
+    g.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_longlong, vp, ctypes.c_size_t, vp, vp]
+    out = ctypes.create_string_buffer(64)
+    assert g(p, 0, p, 0, 0, p, 1 << 20, None, out) == -1                                 # n = 0
+    assert g(p, 0, p, 5, 10, p, 1 << 20, None, out) == -1                                # bad dtype
+    assert g(p, 0, p, 0, 10, None, 0, None, out) == -3                                   # no workspace
+    assert g(p, 0, p, 0, 10, vp(16 + 256), 1 << 20, None, out) == -3                     # misaligned
+
+
+def test_debug_timeout_rejects_bad_limit(lib):
+    f = lib.attn_debug_wait_timeout
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_uint, ctypes.c_void_p]
+    assert f(0, None) == -1
+    assert f(2_000_000, None) == -1

@@ -1,0 +1,216 @@
+"""GPU parity of attn_fwd (through the C ABI) against the FP64 oracle.
+
+Tolerances (max-abs on O): 1e-5 for float32 inputs, 2e-2 for bf16 inputs
+with float32 accumulation.  LSE: float32 rounding of the scaled scores,
+|dLSE| <= 1e-5 * max(1, |LSE|) for float32 and 1e-3 + 2e-6 * |LSE| for bf16.
+Fully masked rows must give O == 0 exactly and LSE == -inf, and no output
+may be NaN.  Large configurations are checked on a seeded row subset that
+always includes each head's first rows, last row and every fully masked row.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = {"f32": 1e-5, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module")
+def eta():
+    import exact_tiled_attention_17_gb300 as m
+    return m
+
+
+def _lse_tol(dtype, ref):
+    a = np.abs(np.where(np.isfinite(ref), ref, 0.0))
+    return 1e-5 * np.maximum(1.0, a) if dtype == "f32" else 1e-3 + 2e-6 * a
+
+
+def run_case(eta, B, H, N, d, dtype, causal, Br=0, Bc=0, mask=None, qk_scale=1.0, seed=0, rows=None,
+             scale=None, qkv=None):
+    if qkv is None:
+        q, k, v = workloads.make_qkv(B, H, N, d, dtype, seed, qk_scale)
+    else:
+        q, k, v = qkv
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dev = torch.device("cuda")
+    o, lse = eta.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal, scale, Br, Bc,
+                          mask.to(dev) if mask is not None else None)
+    torch.cuda.synchronize()
+    assert eta.attn_status() == eta.ATTN_OK
+    o_ref, lse_ref = oracle.attn(q, k, v, causal, scale, key_mask=mask, rows=rows)
+    og = o.double().cpu().numpy().reshape(-1, d)
+    lg = lse.double().cpu().numpy().reshape(-1)
+    if rows is not None:
+        og, lg = og[rows], lg[rows]
+    o_ref = o_ref.reshape(-1, d)
+    lse_ref = lse_ref.reshape(-1)
+    assert not np.isnan(og).any() and not np.isnan(lg).any()
+    err = np.abs(og - o_ref).max()
+    assert err <= TOL_O[dtype], f"max|dO| = {err}"
+    inf_ref = np.isneginf(lse_ref)
+    np.testing.assert_array_equal(np.isneginf(lg), inf_ref)
+    assert np.all(og[inf_ref] == 0.0)
+    fin = ~inf_ref
+    lerr = np.abs(lg[fin] - lse_ref[fin])
+    assert np.all(lerr <= _lse_tol(dtype, lse_ref[fin])), f"max|dLSE| = {lerr.max()}"
+    return err
+
+
+# ---------------- float32 path (CUDA cores) ----------------
+
+def test_fp32_small_config(eta):
+    """1 x 1 x 256 x 64, non-causal, seed 0: max-abs <= 1e-5."""
+    w = workloads.WORKLOADS["fp32_1x1x256x64"]
+    run_case(eta, w.B, w.H, w.N, w.d, "f32", w.causal)
+    assert eta.attn_last_variant().startswith("simt_f32")
+
+
+def test_fp32_worked_example(eta, golden_dir):
+    """The tutorial's 5-score row embedded as a causal problem (q_i = e0,
+    k_j = s_j e0, scale 1, d = 64 with zero padding): row i is the causal
+    prefix of length i+1.  float32 holds 1000..1004 exactly."""
+    import json, os
+    g = json.load(open(os.path.join(golden_dir, "worked_example.json")))
+    s = torch.tensor(g["scores"], dtype=torch.float32)
+    vals = torch.tensor(g["values"], dtype=torch.float32)
+    N, d = 5, 64
+    q = torch.zeros(1, 1, N, d); q[..., 0] = 1.0
+    k = torch.zeros(1, 1, N, d); k[0, 0, :, 0] = s
+    v = torch.zeros(1, 1, N, d); v[0, 0, :, :2] = vals
+    run_case(eta, 1, 1, N, d, "f32", True, scale=1.0, qkv=(q, k, v))
+    o, lse = eta.attn_fwd(q.cuda(), k.cuda(), v.cuda(), True, 1.0)
+    o = o.cpu().double()
+    assert o[0, 0, 0, 0] == 2.0 and o[0, 0, 0, 1] == -1.0 and lse[0, 0, 0].item() == 1000.0
+    e = math.e
+    assert abs(o[0, 0, 1, 0].item() - 2 / (1 + e)) <= 1e-6
+    assert abs(o[0, 0, 1, 1].item() - (3 * e - 1) / (1 + e)) <= 1e-6
+
+
+@pytest.mark.parametrize("N", [1, 5, 63, 65, 129, 300])
+@pytest.mark.parametrize("d", [17, 64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_tails(eta, N, d, causal):
+    run_case(eta, 1, 2, N, d, "f32", causal, seed=N + d)
+
+
+def test_fp32_masked_with_fully_masked_rows(eta):
+    B, H, N, d = 1, 4, 200, 64
+    mask = workloads.make_key_mask(B, H, N, 0.1, seed=3)
+    mask[0, 1, :] = float("-inf")  # one head with no allowed key at all
+    run_case(eta, B, H, N, d, "f32", False, mask=mask, seed=3)
+    run_case(eta, B, H, N, d, "f32", True, mask=mask, seed=3)
+
+
+# ---------------- bf16 path (tcgen05 tensor cores) ----------------
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Bc", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_tiles_small(eta, d, Bc, causal):
+    """Every Bc variant: several query groups, K/V ring wrap-around, ragged tail."""
+    run_case(eta, 1, 3, 1000, d, "bf16", causal, Br=128, Bc=Bc, seed=d + Bc)
+
+
+@pytest.mark.parametrize("N", [1, 5, 127, 128, 129, 255, 256, 257, 511, 513])
+def test_bf16_tails(eta, N):
+    run_case(eta, 2, 2, N, 128, "bf16", N % 2 == 1, seed=N)
+    run_case(eta, 1, 2, N, 64, "bf16", N % 2 == 0, seed=N + 1)
+
+
+@pytest.mark.parametrize("Bc", [64, 128, 256])
+def test_bf16_masked(eta, Bc):
+    B, H, N, d = 1, 4, 700, 128
+    mask = workloads.make_key_mask(B, H, N, 0.05, seed=5)
+    mask[0, 2, :] = float("-inf")
+    run_case(eta, B, H, N, d, "bf16", True, Bc=Bc, mask=mask, seed=5)
+    run_case(eta, B, H, N, d, "bf16", False, Bc=Bc, mask=mask, seed=5)
+
+
+def test_bf16_config2_causal(eta):
+    """4 x 16 x 1024 x 64 causal, every row."""
+    w = workloads.WORKLOADS["bf16_causal_4x16x1024x64"]
+    run_case(eta, w.B, w.H, w.N, w.d, "bf16", w.causal)
+    assert eta.attn_last_variant().startswith("tc_bf16")
+
+
+def test_bf16_config3_full_size(eta):
+    """2 x 16 x 4096 x 128 non-causal at full size, in the benchmark's
+    launch configuration; oracle on a seeded 1/32 row subset."""
+    w = workloads.WORKLOADS["bf16_2x16x4096x128"]
+    rows = workloads.sample_rows(w.B, w.H, w.N, 1 / 32, seed=0)
+    run_case(eta, w.B, w.H, w.N, w.d, "bf16", w.causal, rows=rows)
+
+
+def test_bf16_config5_adversarial(eta):
+    """1 x 32 x 8192 x 128 causal, Q and K x30, 5% -inf key padding with
+    fully masked rows; oracle on a seeded row subset plus every fully
+    masked row."""
+    w = workloads.WORKLOADS["bf16_causal_adv_1x32x8192x128"]
+    q, k, v, mask = workloads.make_inputs(w)
+    # fully masked rows under causality: row i of head h whose keys 0..i are all masked
+    m = mask.numpy().reshape(w.B * w.H, w.N)
+    extra = []
+    for bh in range(w.B * w.H):
+        allowed = np.cumsum(np.isfinite(m[bh]))
+        extra += [bh * w.N + i for i in np.nonzero(allowed == 0)[0]]
+    assert len(extra) > 0
+    rows = workloads.sample_rows(w.B, w.H, w.N, 1 / 256, seed=0, extra=extra)
+    run_case(eta, w.B, w.H, w.N, w.d, "bf16", w.causal, mask=mask, rows=rows, qkv=(q, k, v))
+
+
+def test_bf16_br_bc_variants_match(eta):
+    """Rows are independent: every (Br, Bc) variant the library accepts gives
+    a result within tolerance of the oracle on the same inputs."""
+    B, H, N, d = 1, 2, 600, 64
+    for bc in (64, 128, 256):
+        run_case(eta, B, H, N, d, "bf16", False, Br=128, Bc=bc, seed=9)
+
+
+def test_guard_bands_untouched(eta):
+    """O and LSE written in place inside larger buffers: the canary bands
+    before and after them must be left alone (ragged N, causal)."""
+    B, H, N, d = 1, 3, 333, 128
+    q, k, v = workloads.make_qkv(B, H, N, d, "bf16", 11)
+    dev = torch.device("cuda")
+    n_o, n_l, pad = B * H * N * d, B * H * N, 4096
+    obuf = torch.full((n_o + 2 * pad,), 7.0, dtype=torch.bfloat16, device=dev)
+    lbuf = torch.full((n_l + 2 * pad,), 7.0, dtype=torch.float32, device=dev)
+    o = obuf[pad:pad + n_o].view(B, H, N, d)
+    l = lbuf[pad:pad + n_l].view(B, H, N)
+    eta.attn_fwd(q.to(dev), k.to(dev), v.to(dev), True, 1 / math.sqrt(d), out=o, lse=l)
+    torch.cuda.synchronize()
+    assert torch.all(obuf[:pad] == 7.0) and torch.all(obuf[pad + n_o:] == 7.0)
+    assert torch.all(lbuf[:pad] == 7.0) and torch.all(lbuf[pad + n_l:] == 7.0)
+
+
+def test_host_buffers_end_to_end(eta):
+    """The host-memory path: pinned CPU tensors in, CPU tensors out."""
+    q, k, v = workloads.make_qkv(1, 2, 256, 64, "bf16", 4)
+    o, lse = eta.attn_fwd(q.pin_memory(), k.pin_memory(), v.pin_memory(), False, 0.125)
+    assert o.device.type == "cpu" and lse.device.type == "cpu"
+    o_ref, _ = oracle.attn(q, k, v, False, 0.125)
+    assert np.abs(o.double().numpy() - o_ref).max() <= 2e-2
+
+
+def test_device_timeout_is_reported_and_recovered(eta):
+    """A kernel whose wait can never complete gives up after its limit,
+    records the timeout, and leaves the context usable."""
+    assert eta.attn_status() == eta.ATTN_OK
+    assert eta.attn_debug_wait_timeout(2000) == eta.ATTN_OK
+    assert eta.attn_status() == eta.ATTN_ERR_DEVICE_TIMEOUT
+    assert eta.attn_status() == eta.ATTN_OK   # cleared
+    run_case(eta, 1, 1, 64, 64, "bf16", False)
+
+
+def test_invalid_arguments_on_device(eta):
+    q = torch.zeros(1, 1, 64, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(eta.AttnError) as ei:
+        eta.attn_fwd(q, q, q)
+    assert ei.value.status == eta.ATTN_ERR_UNSUPPORTED
