@@ -103,7 +103,7 @@ int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, i
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == ATTN_BF16) {
         if (d != 64 && d != 128) return kErrUnsupported;
-        if (!((Br == 0 && Bc == 0) || ((Br == 64 || Br == 128) && (Bc == 64 || Bc == 128 || Bc == 256))))
+        if (!((Br == 0 || Br == 64 || Br == 128) && (Bc == 0 || Bc == 64 || Bc == 128 || Bc == 256)))
             return kErrUnsupported;
         int dev = 0, major = 0, minor = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;

@@ -8,25 +8,33 @@
 // unnormalised accumulator that is multiplied by exp(m_old - m_new) when the
 // maximum grows, with one division at the end.
 //
-// GB300 mapping (one CTA per group of NQ consecutive 128-row query tiles of
-// one (batch, head)):
+// GB300 mapping: one CTA per group of NQ consecutive BR-row query tiles of one
+// (batch, head); heaviest groups (largest row index, for causal) launch first.
 //   warp 4*NQ      TMA producer: Q tiles once, then K_j / V_j tiles into a
 //                  ring of NS shared-memory slots (128-byte swizzle).
-//   warp 4*NQ + 1  MMA issuer (one thread): S_q = Q_q K_j^T and
-//                  O_q += P_q V_j on tcgen05, accumulators in tensor memory.
+//   warp 4*NQ + 1  MMA issuer (one thread): S_q = Q_q K_j^T (both operands in
+//                  shared memory) and O_q += P_q V_j (P from tensor memory, V
+//                  MN-major in shared memory) on tcgen05, f32 accumulators in
+//                  tensor memory.
 //   warps 4q..4q+3 softmax warpgroup of query tile q: one thread per row
-//                  (TMEM lane = row).  Reads S_q, applies scale and masks,
-//                  updates (m, l), rescales O_q in TMEM when needed, writes
-//                  P_q as bf16 back over S_q's columns (the A operand of the
-//                  next MMA comes straight from TMEM), then the epilogue.
+//                  (tensor-memory lane = row).  Reads S_q, applies scale and
+//                  masks, updates (m, l), rescales O_q in tensor memory when
+//                  needed, writes P_q as bf16 back over S_q's columns, then
+//                  the epilogue (normalise, bf16, TMA store; LSE).
 // The MMA issue order S_0(j+1) after PV_0(j), S_1(j+1) after PV_1(j) lets the
-// tensor pipe work on one tile while the other tile's softmax runs.
+// tensor pipe work on one tile while the other tile's softmax runs.  With two
+// query tiles the softmax warpgroups take 224 registers per thread with
+// setmaxnreg and the producer/MMA warpgroup gives its share back.
+//
+// BR = 64 uses M = 64 MMAs, whose accumulator rows r sit in tensor-memory lane
+// 32*(r/16) + r%16: lanes 0..15 of each warp carry rows, lanes 16..31 idle.
 //
 // The reference maximum is moved only when the tile maximum exceeds it by
 // more than kRescaleThresh (log2 units): exact up to rounding because a / l
 // does not depend on the reference point, and p = 2^(x - m) stays <= 2^8.
-// The denominator l sums the same bf16-rounded p that enter P V, so the
-// normalised weights are the ones actually applied.
+// Two denominators are kept: the sum of the bf16-rounded p that actually
+// enter P V (normalises O, so the applied weights sum to one) and the float32
+// sum of p (gives the LSE).
 #include <cuda_bf16.h>
 #include <cstdio>
 
@@ -41,9 +49,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThresh = 8.0f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
-template <int D, int BC, int NQ>
+template <int D, int BR, int BC, int NQ>
 struct TcShape {
-    static constexpr int BR = 128;
     static constexpr int CB = D / 64;               // 128-byte column blocks per row
     static constexpr int Q_BYTES = BR * D * 2;      // one Q (or O staging) tile
     static constexpr int SLOT_BYTES = BC * D * 2;   // one K or V tile
@@ -58,7 +65,13 @@ struct TcShape {
     static constexpr int SOFTMAX_WARPS = 4 * NQ;
     static constexpr int WARP_TMA = SOFTMAX_WARPS;
     static constexpr int WARP_MMA = SOFTMAX_WARPS + 1;
-    static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+    // Two query tiles: a third full warpgroup (TMA, MMA, 2 idle) so that
+    // setmaxnreg can move registers between whole warpgroups.
+    static constexpr bool SPLIT_REGS = (NQ == 2);
+    static constexpr int THREADS = SPLIT_REGS ? 384 : 32 * (SOFTMAX_WARPS + 2);
+    static constexpr int LAUNCH_REGS = 168;          // 65536 / 384, rounded down to 8
+    static constexpr int REGS_SOFTMAX = 224;
+    static constexpr int REGS_OTHER = 56;            // 2*128*224 + 128*56 == 384*168
     // shared memory layout (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * Q_BYTES;
@@ -79,17 +92,20 @@ struct TcShape {
     __host__ __device__ static constexpr int o_col(int q) { return NQ * BC + q * D; }
 
     static_assert(D == 64 || D == 128, "head dim");
+    static_assert(BR == 64 || BR == 128, "query tile");
     static_assert(BC == 64 || BC == 128 || BC == 256, "key tile");
     static_assert(TMEM_USED <= 512, "tensor memory budget");
     // A 512-column allocation must never wait for another resident CTA.
     static_assert(TMEM_COLS < 512 || SMEM_BYTES > 116 * 1024, "one CTA per SM for full TMEM");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(!SPLIT_REGS || 2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER == THREADS * LAUNCH_REGS,
+                  "register split must equal the launch allocation");
 };
 
 struct TcParams {
     int N;              // sequence length
     int BH;             // B * H
-    int num_qg;         // query groups (NQ * 128 rows) per head
+    int num_qg;         // query groups (NQ * BR rows) per head
     int causal;
     float scale_log2;   // scale * log2(e)
     const float *key_mask;  // [BH][N] additive, or null
@@ -97,19 +113,19 @@ struct TcParams {
     int *err;               // device error word
 };
 
-template <int D, int BC, int NQ, bool MASKED>
-__global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
+template <int D, int BR, int BC, int NQ, bool MASKED>
+__global__ void __launch_bounds__(TcShape<D, BR, BC, NQ>::THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                        const TcParams p) {
-    using S = TcShape<D, BC, NQ>;
+    using S = TcShape<D, BR, BC, NQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- work item: heaviest query groups (largest rows) launch first ----
+    // ---- work item ----
     const int lin = blockIdx.x;
     const int qg = p.num_qg - 1 - lin / p.BH;
     const int bh = lin % p.BH;
@@ -119,11 +135,11 @@ __global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
     int nkv_max = 0;
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
-        r0[q] = (qg * NQ + q) * 128;
+        r0[q] = (qg * NQ + q) * BR;
         if (r0[q] >= N) {
             nkv[q] = 0;
         } else if (p.causal) {
-            const int last_row = min(r0[q] + 127, N - 1);
+            const int last_row = min(r0[q] + BR - 1, N - 1);
             nkv[q] = min(nkv_all, last_row / BC + 1);
         } else {
             nkv[q] = nkv_all;
@@ -161,138 +177,150 @@ __global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == S::WARP_TMA) {
-        // ------------------------------------------------------------------
-        // TMA producer
-        // ------------------------------------------------------------------
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            tma_prefetch_desc(&tm_o);
-            const uint64_t pol_kv = l2_policy_evict_last();   // K/V are re-read by every query group
-            const uint64_t pol_q = l2_policy_evict_first();   // Q is read once
-            for (int q = 0; q < NQ; ++q) {
-                if (nkv[q] == 0) continue;
-                mbar_arrive_expect_tx(bar(S::BAR_QFULL + q), S::Q_BYTES);
+    if (warp >= S::SOFTMAX_WARPS) {
+        if constexpr (S::SPLIT_REGS) regs_dec<S::REGS_OTHER>();
+        if (warp == S::WARP_TMA) {
+            // --------------------------------------------------------------
+            // TMA producer
+            // --------------------------------------------------------------
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+                tma_prefetch_desc(&tm_o);
+                const uint64_t pol_kv = l2_policy_evict_last();   // K/V are re-read by every query group
+                const uint64_t pol_q = l2_policy_evict_first();   // Q is read once
+                for (int q = 0; q < NQ; ++q) {
+                    if (nkv[q] == 0) continue;
+                    mbar_arrive_expect_tx(bar(S::BAR_QFULL + q), S::Q_BYTES);
 #pragma unroll
-                for (int cb = 0; cb < S::CB; ++cb)
-                    tma_load_3d_hint(sQ + q * S::Q_BYTES + cb * (128 * 128), &tm_q, bar(S::BAR_QFULL + q),
-                                     cb * 64, r0[q], bh, pol_q);
-            }
-            const int T = 2 * nkv_max;  // K_0 V_0 K_1 V_1 ...
-            int issued = 0;
-            for (int t = 0; t < T; ++t) {
-                const int slot = t % S::NS, round = t / S::NS;
-                if (round > 0 &&
-                    !mbar_wait(bar(S::BAR_EMPTY + slot), (round - 1) & 1, abort_flag, p.err, 1))
-                    break;
-                mbar_arrive_expect_tx(bar(S::BAR_FULL + slot), S::SLOT_BYTES);
-                const CUtensorMap *m = (t & 1) ? &tm_v : &tm_k;
-                const int j = t >> 1;
+                    for (int cb = 0; cb < S::CB; ++cb)
+                        tma_load_3d_hint(sQ + q * S::Q_BYTES + cb * (BR * 128), &tm_q, bar(S::BAR_QFULL + q),
+                                         cb * 64, r0[q], bh, pol_q);
+                }
+                const int T = 2 * nkv_max;  // K_0 V_0 K_1 V_1 ...
+                int issued = 0;
+                for (int t = 0; t < T; ++t) {
+                    const int slot = t % S::NS, round = t / S::NS;
+                    if (round > 0 &&
+                        !mbar_wait(bar(S::BAR_EMPTY + slot), (round - 1) & 1, abort_flag, p.err, 1))
+                        break;
+                    mbar_arrive_expect_tx(bar(S::BAR_FULL + slot), S::SLOT_BYTES);
+                    const CUtensorMap *m = (t & 1) ? &tm_v : &tm_k;
+                    const int j = t >> 1;
 #pragma unroll
-                for (int cb = 0; cb < S::CB; ++cb)
-                    tma_load_3d_hint(sRing + slot * S::SLOT_BYTES + cb * (BC * 128), m, bar(S::BAR_FULL + slot),
-                                     cb * 64, j * BC, bh, pol_kv);
-                issued = t + 1;
+                    for (int cb = 0; cb < S::CB; ++cb)
+                        tma_load_3d_hint(sRing + slot * S::SLOT_BYTES + cb * (BC * 128), m,
+                                         bar(S::BAR_FULL + slot), cb * 64, j * BC, bh, pol_kv);
+                    issued = t + 1;
+                }
+                // Drain: every copy this thread started has landed before the
+                // CTA may exit (normally already true).
+                for (int t = max(0, issued - S::NS); t < issued; ++t)
+                    mbar_wait(bar(S::BAR_FULL + t % S::NS), (t / S::NS) & 1, abort_flag, p.err, 2);
+                for (int q = 0; q < NQ; ++q)
+                    if (nkv[q] > 0) mbar_wait(bar(S::BAR_QFULL + q), 0, abort_flag, p.err, 3);
             }
-            // Drain: every copy this thread started has landed before the CTA
-            // may exit (normally already true).
-            for (int t = max(0, issued - S::NS); t < issued; ++t)
-                mbar_wait(bar(S::BAR_FULL + t % S::NS), (t / S::NS) & 1, abort_flag, p.err, 2);
-            for (int q = 0; q < NQ; ++q)
-                if (nkv[q] > 0) mbar_wait(bar(S::BAR_QFULL + q), 0, abort_flag, p.err, 3);
-        }
-        __syncwarp();
-    } else if (warp == S::WARP_MMA) {
-        // ------------------------------------------------------------------
-        // MMA issuer (one thread)
-        // ------------------------------------------------------------------
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(128, BC, false, false);  // Q, K both K-major
-            constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);    // P (TMEM), V MN-major
-            bool ok = true;
-            for (int q = 0; q < NQ && ok; ++q)
-                if (nkv[q] > 0) ok = mbar_wait(bar(S::BAR_QFULL + q), 0, abort_flag, p.err, 10);
+            __syncwarp();
+        } else if (warp == S::WARP_MMA) {
+            // --------------------------------------------------------------
+            // MMA issuer (one thread)
+            // --------------------------------------------------------------
+            if (lane == 0) {
+                constexpr uint32_t idesc_s = idesc_bf16_f32(BR, BC, false, false);  // Q, K both K-major
+                constexpr uint32_t idesc_o = idesc_bf16_f32(BR, D, false, true);    // P (TMEM), V MN-major
+                bool ok = true;
+                for (int q = 0; q < NQ && ok; ++q)
+                    if (nkv[q] > 0) ok = mbar_wait(bar(S::BAR_QFULL + q), 0, abort_flag, p.err, 10);
 
-            auto issue_s = [&](int q, int j) {
-                const uint32_t kslot = sRing + ((2 * j) % S::NS) * S::SLOT_BYTES;
-                const uint32_t qbuf = sQ + q * S::Q_BYTES;
+                auto issue_s = [&](int q, int j) {
+                    const uint32_t kslot = sRing + ((2 * j) % S::NS) * S::SLOT_BYTES;
+                    const uint32_t qbuf = sQ + q * S::Q_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const int cb = kk >> 2, off = (kk & 3) * 32;
-                    const uint64_t a = sdesc_sw128(qbuf + cb * (128 * 128) + off, 16, 1024);
-                    const uint64_t b = sdesc_sw128(kslot + cb * (BC * 128) + off, 16, 1024);
-                    mma_bf16_ss(tmem + S::s_col(q), a, b, idesc_s, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(bar(S::BAR_SFULL + q));
-            };
-            auto issue_pv = [&](int q, int j) {
-                const uint32_t vslot = sRing + ((2 * j + 1) % S::NS) * S::SLOT_BYTES;
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int cb = kk >> 2, off = (kk & 3) * 32;
+                        const uint64_t a = sdesc_sw128(qbuf + cb * (BR * 128) + off, 16, 1024);
+                        const uint64_t b = sdesc_sw128(kslot + cb * (BC * 128) + off, 16, 1024);
+                        mma_bf16_ss(tmem + S::s_col(q), a, b, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(S::BAR_SFULL + q));
+                };
+                auto issue_pv = [&](int q, int j) {
+                    const uint32_t vslot = sRing + ((2 * j + 1) % S::NS) * S::SLOT_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BC / 16; ++kk) {
-                    const uint64_t b = sdesc_sw128(vslot + kk * 2048, BC * 128, 1024);
-                    mma_bf16_ts(tmem + S::o_col(q), tmem + S::s_col(q) + kk * 8, b, idesc_o,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                }
-            };
+                    for (int kk = 0; kk < BC / 16; ++kk) {
+                        const uint64_t b = sdesc_sw128(vslot + kk * 2048, BC * 128, 1024);
+                        mma_bf16_ts(tmem + S::o_col(q), tmem + S::s_col(q) + kk * 8, b, idesc_o,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                };
 
-            if (ok && nkv_max > 0) {
-                ok = mbar_wait(bar(S::BAR_FULL + 0), 0, abort_flag, p.err, 11);  // K_0
-                if (ok) {
-                    tc_fence_after();
-                    for (int q = 0; q < NQ; ++q)
-                        if (nkv[q] > 0) issue_s(q, 0);
-                    tc_commit(bar(S::BAR_EMPTY + 0));
-                }
-            }
-            for (int j = 0; ok && j < nkv_max; ++j) {
-                const int tv = 2 * j + 1;
-                if (!mbar_wait(bar(S::BAR_FULL + tv % S::NS), (tv / S::NS) & 1, abort_flag, p.err, 12)) break;
-                tc_fence_after();
-                bool k_ready = false;
-                const int tk = 2 * j + 2;
-                for (int q = 0; q < NQ && ok; ++q) {
-                    if (j >= nkv[q]) continue;
-                    if (!mbar_wait(bar(S::BAR_PFULL + q), j & 1, abort_flag, p.err, 13)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_pv(q, j);
-                    if (j == nkv[q] - 1) tc_commit(bar(S::BAR_OFULL + q));
-                    if (j + 1 < nkv[q]) {
-                        if (!k_ready) {
-                            if (!mbar_wait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, abort_flag, p.err, 14)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            k_ready = true;
-                        }
-                        issue_s(q, j + 1);
+                if (ok && nkv_max > 0) {
+                    ok = mbar_wait(bar(S::BAR_FULL + 0), 0, abort_flag, p.err, 11);  // K_0
+                    if (ok) {
+                        tc_fence_after();
+                        for (int q = 0; q < NQ; ++q)
+                            if (nkv[q] > 0) issue_s(q, 0);
+                        tc_commit(bar(S::BAR_EMPTY + 0));
                     }
                 }
-                tc_commit(bar(S::BAR_EMPTY + tv % S::NS));            // V_j slot
-                if (k_ready) tc_commit(bar(S::BAR_EMPTY + tk % S::NS));  // K_{j+1} slot
+                for (int j = 0; ok && j < nkv_max; ++j) {
+                    const int tv = 2 * j + 1;
+                    if (!mbar_wait(bar(S::BAR_FULL + tv % S::NS), (tv / S::NS) & 1, abort_flag, p.err, 12)) break;
+                    tc_fence_after();
+                    bool k_ready = false;
+                    const int tk = 2 * j + 2;
+                    for (int q = 0; q < NQ && ok; ++q) {
+                        if (j >= nkv[q]) continue;
+                        if (!mbar_wait(bar(S::BAR_PFULL + q), j & 1, abort_flag, p.err, 13)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(q, j);
+                        if (j == nkv[q] - 1) tc_commit(bar(S::BAR_OFULL + q));
+                        if (j + 1 < nkv[q]) {
+                            if (!k_ready) {
+                                if (!mbar_wait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, abort_flag, p.err,
+                                               14)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                k_ready = true;
+                            }
+                            issue_s(q, j + 1);
+                        }
+                    }
+                    tc_commit(bar(S::BAR_EMPTY + tv % S::NS));               // V_j slot
+                    if (k_ready) tc_commit(bar(S::BAR_EMPTY + tk % S::NS));  // K_{j+1} slot
+                }
+                // Every MMA issued has completed before tensor memory is released.
+                tc_commit(bar(S::BAR_DONE));
+                mbar_wait(bar(S::BAR_DONE), 0, abort_flag, p.err, 15);
             }
-            // Every MMA issued has completed before tensor memory is released.
-            tc_commit(bar(S::BAR_DONE));
-            mbar_wait(bar(S::BAR_DONE), 0, abort_flag, p.err, 15);
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------------
         // Softmax warpgroup of query tile q
         // ------------------------------------------------------------------
+        if constexpr (S::SPLIT_REGS) regs_inc<S::REGS_SOFTMAX>();
         const int q = warp >> 2;
         const int wq = warp & 3;
-        const int row_in = wq * 32 + lane;
+        // Row of this thread.  M = 128: lane l of warp w holds row 32w + l.
+        // M = 64: lanes 0..15 of warp w hold rows 16w .. 16w+15.
+        const bool active = (BR == 128) || (lane < 16);
+        const int row_in = (BR == 128) ? wq * 32 + lane : wq * 16 + (lane & 15);
         const int row = r0[q] + row_in;
         const uint32_t t_lane = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + t_lane + S::s_col(q);
         const uint32_t tO = tmem + t_lane + S::o_col(q);
         const float sl2 = p.scale_log2;
         const float *mrow = MASKED ? p.key_mask + static_cast<size_t>(bh) * N : nullptr;
-        float m = kNegInf;  // reference maximum, log2 units
-        float l = 0.f;
+        float m = kNegInf;    // reference maximum, log2 units
+        float l_exact = 0.f;  // sum of float32 p (for LSE)
+        float l_round = 0.f;  // sum of the bf16-rounded p used in P V (normalises O)
         bool ok = true;
 
         for (int j = 0; j < nkv[q]; ++j) {
@@ -303,7 +331,7 @@ __global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
             // diagonal, or any tile when a key mask is given.
             const bool edge = MASKED || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0[q]);
 
-            // Transform one loaded 32-column chunk into log2-domain scores
+            // One loaded 32-column chunk -> log2-domain scores
             // x = s*scale*log2(e) (+ mask*log2(e)), -inf where not allowed.
             auto mask_chunk = [&](int c, uint32_t *r) {
 #pragma unroll
@@ -315,26 +343,31 @@ __global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
                     r[e] = __float_as_uint(allowed ? x : kNegInf);
                 }
             };
+            auto chunk_max = [&](const uint32_t *r, float mx) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) mx = fmax3(mx, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                return mx;
+            };
             // p = 2^(x - m_use) for one chunk, packed to bf16 pairs and written
             // over S's first BC/2 columns (chunk c -> columns 16c .. 16c+15,
             // never ahead of the chunks still to be read).
-            auto exp_chunk = [&](int c, const uint32_t *r, float m_use, float &rs) {
+            auto exp_chunk = [&](int c, const uint32_t *r, uint64_t negm2, uint64_t &ls2, uint64_t &lr2) {
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float x0 = __uint_as_float(r[2 * e]);
-                    const float x1 = __uint_as_float(r[2 * e + 1]);
-                    const float p0 = edge ? ex2(x0 - m_use) : ex2(fmaf(x0, sl2, -m_use));
-                    const float p1 = edge ? ex2(x1 - m_use) : ex2(fmaf(x1, sl2, -m_use));
-                    pk[e] = pack_bf16x2(p0, p1);
-                    rs += bf16lo_to_f32(pk[e]) + bf16hi_to_f32(pk[e]);
+                    const uint64_t xx = f2_pack(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                    const uint64_t y = edge ? f2_add(xx, negm2) : f2_fma(xx, sl2x2, negm2);
+                    float y0, y1;
+                    f2_unpack(y, y0, y1);
+                    const float p0 = ex2(y0), p1 = ex2(y1);
+                    uint32_t w = pack_bf16x2(p0, p1);
+                    if (!active) w = 0u;
+                    pk[e] = w;
+                    ls2 = f2_add(ls2, f2_pack(p0, p1));
+                    lr2 = f2_add(lr2, f2_pack(bf16lo_to_f32(w), bf16hi_to_f32(w)));
                 }
                 tmem_st16(tS + 16 * c, pk);
-            };
-            auto chunk_max = [&](const uint32_t *r, float mx) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
-                return mx;
             };
 
             constexpr bool kTwoPass = BC > 128;   // 256 columns do not fit in registers
@@ -370,11 +403,12 @@ __global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
                 if (!edge) mx *= sl2;
             }
 
-            const float m_new = (mx > m + kRescaleThresh) ? mx : m;
+            const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
             const bool moved = (m_new != m);
             const float alpha = moved ? ex2(m - m_new) : 1.f;
             const float m_use = (m_new == kNegInf) ? 0.f : m_new;
             if (j > 0 && __any_sync(0xffffffffu, moved)) {
+                const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -382,16 +416,23 @@ __global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
                     tmem_ld_wait();
                     reg_fence32(o);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    for (int e = 0; e < 32; e += 2) {
+                        const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+                        float v0, v1;
+                        f2_unpack(v, v0, v1);
+                        o[e] = __float_as_uint(v0);
+                        o[e + 1] = __float_as_uint(v1);
+                    }
                     tmem_st32(tO + 32 * c, o);
                 }
             }
             m = m_new;
 
-            float rs = 0.f;
+            const uint64_t negm2 = f2_pack(-m_use, -m_use);
+            uint64_t ls2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
             if constexpr (!kTwoPass) {
 #pragma unroll
-                for (int c = 0; c < BC / 32; ++c) exp_chunk(c, sr + 32 * c, m_use, rs);
+                for (int c = 0; c < BC / 32; ++c) exp_chunk(c, sr + 32 * c, negm2, ls2, lr2);
             } else {
 #pragma unroll 1
                 for (int c = 0; c < BC / 32; ++c) {
@@ -399,10 +440,14 @@ __global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
                     tmem_ld_wait();
                     reg_fence32(sr);
                     if (edge) mask_chunk(c, sr);
-                    exp_chunk(c, sr, m_use, rs);
+                    exp_chunk(c, sr, negm2, ls2, lr2);
                 }
             }
-            l = l * alpha + rs;
+            float s0, s1, t0, t1;
+            f2_unpack(ls2, s0, s1);
+            f2_unpack(lr2, t0, t1);
+            l_exact = l_exact * alpha + (s0 + s1);
+            l_round = l_round * alpha + (t0 + t1);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(S::BAR_PFULL + q));
@@ -412,7 +457,9 @@ __global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
         if (nkv[q] > 0) {
             if (ok) ok = mbar_wait(bar(S::BAR_OFULL + q), 0, abort_flag, p.err, 21);
             tc_fence_after();
-            const float inv = (l > 0.f) ? 1.f / l : 0.f;
+            const bool any = (l_exact > 0.f) && (l_round > 0.f);
+            const float inv = any ? 1.f / l_round : 0.f;
+            const uint64_t inv2 = f2_pack(inv, inv);
             const uint32_t stage = sQ + q * S::Q_BYTES;  // Q_q is no longer read
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -422,30 +469,36 @@ __global__ void __launch_bounds__(TcShape<D, BC, NQ>::THREADS, 1)
                 reg_fence32(o);
                 uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-                const int cb = c >> 1;
+                for (int e = 0; e < 16; ++e) {
+                    const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2);
+                    float v0, v1;
+                    f2_unpack(v, v0, v1);
+                    w[e] = pack_bf16x2(v0, v1);
+                }
+                if (active) {
+                    const int cb = c >> 1;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int ch = (c & 1) * 4 + k;  // 16-byte chunk within the 128-byte row
-                    const uint32_t addr = stage + cb * (128 * 128) + row_in * 128 + ((ch ^ (row_in & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * k]),
-                                 "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
-                                 : "memory");
+                    for (int k = 0; k < 4; ++k) {
+                        const int ch = (c & 1) * 4 + k;  // 16-byte chunk within the 128-byte row
+                        const uint32_t addr =
+                            stage + cb * (BR * 128) + row_in * 128 + ((ch ^ (row_in & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * k]),
+                                     "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
+                                     : "memory");
+                    }
                 }
             }
             fence_proxy_async_smem();
             named_bar_sync(1 + q, 128);
-            if (row_in == 0 && !*abort_flag) {
+            if (wq == 0 && lane == 0 && !*abort_flag) {
 #pragma unroll
                 for (int cb = 0; cb < S::CB; ++cb)
-                    tma_store_3d(&tm_o, stage + cb * (128 * 128), cb * 64, r0[q], bh);
+                    tma_store_3d(&tm_o, stage + cb * (BR * 128), cb * 64, r0[q], bh);
                 tma_store_commit();
                 tma_store_wait_read0();
             }
-            if (p.lse != nullptr && row < N) {
-                p.lse[static_cast<size_t>(bh) * N + row] =
-                    (l > 0.f) ? (m + log2f(l)) * kLn2 : kNegInf;
+            if (active && p.lse != nullptr && row < N) {
+                p.lse[static_cast<size_t>(bh) * N + row] = any ? (m + log2f(l_exact)) * kLn2 : kNegInf;
             }
         }
     }
@@ -471,27 +524,34 @@ bool make_map(CUtensorMap *m, const void *base, int D, int N, int BH, int box_ro
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int BC, int NQ, bool MASKED>
+template <int D, int BR, int BC, int NQ, bool MASKED>
 int launch_variant(const void *Q, const void *K, const void *V, void *O, float *LSE, int BH, int N,
                    int causal, float scale, const float *key_mask, cudaStream_t stream) {
-    using S = TcShape<D, BC, NQ>;
-    auto kern = attn_fwd_tc_kernel<D, BC, NQ, MASKED>;
+    using S = TcShape<D, BR, BC, NQ>;
+    auto kern = attn_fwd_tc_kernel<D, BR, BC, NQ, MASKED>;
     static int attr_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
     if (attr_device != dev) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES) != cudaSuccess)
             return kErrCuda;
+        if (S::SPLIT_REGS) {
+            // setmaxnreg moves registers within the launch allocation; the split
+            // above is exact only for this per-thread count.
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return kErrCuda;
+            if (fa.numRegs != S::LAUNCH_REGS) return kErrUnsupported;
+        }
         attr_device = dev;
     }
     CUtensorMap tq, tk, tv, to;
-    if (!make_map(&tq, Q, D, N, BH, 128) || !make_map(&tk, K, D, N, BH, BC) || !make_map(&tv, V, D, N, BH, BC) ||
-        !make_map(&to, O, D, N, BH, 128))
+    if (!make_map(&tq, Q, D, N, BH, BR) || !make_map(&tk, K, D, N, BH, BC) || !make_map(&tv, V, D, N, BH, BC) ||
+        !make_map(&to, O, D, N, BH, BR))
         return kErrCuda;
     TcParams p;
     p.N = N;
     p.BH = BH;
-    p.num_qg = (N + NQ * 128 - 1) / (NQ * 128);
+    p.num_qg = (N + NQ * BR - 1) / (NQ * BR);
     p.causal = causal;
     p.scale_log2 = scale * kLog2e;
     p.key_mask = key_mask;
@@ -504,16 +564,28 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
-template <int D, int BC>
-int launch_dbc(const void *Q, const void *K, const void *V, void *O, float *LSE, int BH, int N, int causal,
-               float scale, const float *key_mask, cudaStream_t stream, const char **variant) {
+template <int D, int BR, int BC>
+int launch_shape(const void *Q, const void *K, const void *V, void *O, float *LSE, int BH, int N, int causal,
+                 float scale, const float *key_mask, cudaStream_t stream, const char **variant) {
     constexpr int NQ = (2 * (BC + D) <= 512) ? 2 : 1;
-    static char name[64];
-    snprintf(name, sizeof(name), "tc_bf16_d%d_br128_bc%d_nq%d%s", D, BC, NQ, key_mask ? "_mask" : "");
+    static char names[2][64];
+    char *name = names[key_mask ? 1 : 0];
+    snprintf(name, 64, "tc_bf16_d%d_br%d_bc%d_nq%d%s", D, BR, BC, NQ, key_mask ? "_mask" : "");
     if (variant) *variant = name;
     if (key_mask)
-        return launch_variant<D, BC, NQ, true>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream);
-    return launch_variant<D, BC, NQ, false>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream);
+        return launch_variant<D, BR, BC, NQ, true>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream);
+    return launch_variant<D, BR, BC, NQ, false>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream);
+}
+
+template <int D, int BR>
+int launch_br(int Bc, const void *Q, const void *K, const void *V, void *O, float *LSE, int BH, int N, int causal,
+              float scale, const float *key_mask, cudaStream_t stream, const char **variant) {
+    switch (Bc) {
+        case 64: return launch_shape<D, BR, 64>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+        case 128: return launch_shape<D, BR, 128>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+        case 256: return launch_shape<D, BR, 256>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+        default: return kErrUnsupported;
+    }
 }
 
 }  // namespace
@@ -521,18 +593,13 @@ int launch_dbc(const void *Q, const void *K, const void *V, void *O, float *LSE,
 int launch_fwd_tc_bf16(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
                        int d, int causal, float scale, int Br, int Bc, const float *key_mask,
                        cudaStream_t stream, const char **variant) {
-    if (Br == 0 && Bc == 0) { Br = 128; Bc = 128; }
-    if (Br != 128) return kErrUnsupported;
+    if (Br == 0) Br = 128;
+    if (Bc == 0) Bc = 128;
     const int BH = B * H;
-    if (d == 64) {
-        if (Bc == 64) return launch_dbc<64, 64>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
-        if (Bc == 128) return launch_dbc<64, 128>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
-        if (Bc == 256) return launch_dbc<64, 256>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
-    } else if (d == 128) {
-        if (Bc == 64) return launch_dbc<128, 64>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
-        if (Bc == 128) return launch_dbc<128, 128>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
-        if (Bc == 256) return launch_dbc<128, 256>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
-    }
+    if (d == 64 && Br == 128) return launch_br<64, 128>(Bc, Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+    if (d == 64 && Br == 64) return launch_br<64, 64>(Bc, Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+    if (d == 128 && Br == 128) return launch_br<128, 128>(Bc, Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
+    if (d == 128 && Br == 64) return launch_br<128, 64>(Bc, Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, variant);
     return kErrUnsupported;
 }
 

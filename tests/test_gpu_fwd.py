@@ -111,11 +111,13 @@ def test_fp32_masked_with_fully_masked_rows(eta):
 # ---------------- bf16 path (tcgen05 tensor cores) ----------------
 
 @pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Br", [64, 128])
 @pytest.mark.parametrize("Bc", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bf16_tiles_small(eta, d, Bc, causal):
-    """Every Bc variant: several query groups, K/V ring wrap-around, ragged tail."""
-    run_case(eta, 1, 3, 1000, d, "bf16", causal, Br=128, Bc=Bc, seed=d + Bc)
+def test_bf16_tiles_small(eta, d, Br, Bc, causal):
+    """Every (Br, Bc) variant: several query groups, K/V ring wrap-around, ragged tail."""
+    run_case(eta, 1, 3, 1000, d, "bf16", causal, Br=Br, Bc=Bc, seed=d + Bc + Br)
+    assert f"_br{Br}_bc{Bc}_" in eta.attn_last_variant()
 
 
 @pytest.mark.parametrize("N", [1, 5, 127, 128, 129, 255, 256, 257, 511, 513])
@@ -165,12 +167,37 @@ def test_bf16_config5_adversarial(eta):
     run_case(eta, w.B, w.H, w.N, w.d, "bf16", w.causal, mask=mask, rows=rows, qkv=(q, k, v))
 
 
-def test_bf16_br_bc_variants_match(eta):
-    """Rows are independent: every (Br, Bc) variant the library accepts gives
-    a result within tolerance of the oracle on the same inputs."""
-    B, H, N, d = 1, 2, 600, 64
-    for bc in (64, 128, 256):
-        run_case(eta, B, H, N, d, "bf16", False, Br=128, Bc=bc, seed=9)
+@pytest.mark.parametrize("Br,Bc", workloads.SWEEP_TILES)
+def test_bf16_tile_sweep_config4(eta, Br, Bc):
+    """The tile-size sweep shape: 1 x 8 x 4096 x 64 non-causal, every
+    (Br, Bc) in {64,128} x {64,128,256}; oracle on a seeded row subset."""
+    w = workloads.WORKLOADS["bf16_sweep_1x8xNx64"]
+    rows = workloads.sample_rows(w.B, w.H, w.N, 1 / 64, seed=Br + Bc)
+    run_case(eta, w.B, w.H, w.N, w.d, "bf16", w.causal, Br=Br, Bc=Bc, rows=rows)
+
+
+@pytest.mark.parametrize("N", workloads.SWEEP_N)
+def test_bf16_length_sweep_config4(eta, N):
+    """The sequence-length sweep shape: 1 x 8 x N x 64, N = 128 .. 16384,
+    default tiles; oracle on a seeded row subset (all rows for small N)."""
+    w = workloads.WORKLOADS["bf16_sweep_1x8xNx64"]
+    frac = 1.0 if N <= 1024 else 2048 / (w.B * w.H * N)
+    rows = None if frac >= 1.0 else workloads.sample_rows(w.B, w.H, N, frac, seed=N)
+    run_case(eta, w.B, w.H, N, w.d, "bf16", w.causal, rows=rows, seed=0)
+
+
+def test_bf16_br_variants_agree(eta):
+    """Rows are independent, so Br (rows per tile) must not change any
+    result bit for a fixed Bc: the per-row arithmetic is the same."""
+    q, k, v = workloads.make_qkv(1, 2, 777, 128, "bf16", 9)
+    dev = torch.device("cuda")
+    outs = []
+    for br in (64, 128):
+        o, l = eta.attn_fwd(q.to(dev), k.to(dev), v.to(dev), True, 1 / math.sqrt(128), br, 128)
+        outs.append((o.clone(), l.clone()))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
 
 
 def test_guard_bands_untouched(eta):
