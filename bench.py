@@ -168,7 +168,7 @@ def run_reference(args):
     cores = oracle.default_threads()
     row_flops = 4.0 * w.N * w.d
     # each step: a bounded sample of rows sized so the whole run ends in minutes
-    per_step_rows = 16 * cores
+    per_step_rows = 4 * cores
     g = torch.Generator().manual_seed(7)
     times = []
     for s in range(args.warmup + args.steps):
