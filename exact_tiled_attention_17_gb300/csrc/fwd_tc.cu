@@ -23,7 +23,7 @@
 //                  the epilogue (normalise, bf16, TMA store; LSE).
 // The MMA issue order S_0(j+1) after PV_0(j), S_1(j+1) after PV_1(j) lets the
 // tensor pipe work on one tile while the other tile's softmax runs.  With two
-// query tiles the softmax warpgroups take 224 registers per thread with
+// query tiles the softmax warpgroups take 208 registers per thread with
 // setmaxnreg and the producer/MMA warpgroup gives its share back.
 //
 // BR = 64 uses M = 64 MMAs, whose accumulator rows r sit in tensor-memory lane
@@ -49,13 +49,15 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThresh = 8.0f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
-template <int D, int BR, int BC, int NQ>
+template <int D, int BR, int BC, int NQ, bool MASKED>
 struct TcShape {
     static constexpr int CB = D / 64;               // 128-byte column blocks per row
     static constexpr int Q_BYTES = BR * D * 2;      // one Q (or O staging) tile
     static constexpr int SLOT_BYTES = BC * D * 2;   // one K or V tile
-    static constexpr int SMEM_BUDGET = 200 * 1024;
-    static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES) / SLOT_BYTES;
+    static constexpr int SMEM_BUDGET = 225 * 1024;  // leaves room for barriers and alignment
+    // key mask of the current tile in log2 units, double-buffered per query tile
+    static constexpr int MASK_BYTES = MASKED ? NQ * 2 * BC * 4 : 0;
+    static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES - MASK_BYTES) / SLOT_BYTES;
     static constexpr int NS = NS_RAW > 8 ? 8 : (NS_RAW < 2 ? 2 : NS_RAW);
     static constexpr int TMEM_USED = NQ * (BC + D);
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32
@@ -70,12 +72,13 @@ struct TcShape {
     static constexpr bool SPLIT_REGS = (NQ == 2);
     static constexpr int THREADS = SPLIT_REGS ? 384 : 32 * (SOFTMAX_WARPS + 2);
     static constexpr int LAUNCH_REGS = 168;          // 65536 / 384, rounded down to 8
-    static constexpr int REGS_SOFTMAX = 224;
-    static constexpr int REGS_OTHER = 56;            // 2*128*224 + 128*56 == 384*168
+    static constexpr int REGS_SOFTMAX = 208;
+    static constexpr int REGS_OTHER = 88;            // 2*128*208 + 128*88 == 384*168
     // shared memory layout (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * Q_BYTES;
-    static constexpr int OFF_BAR = OFF_RING + NS * SLOT_BYTES;
+    static constexpr int OFF_MASK = OFF_RING + NS * SLOT_BYTES;
+    static constexpr int OFF_BAR = OFF_MASK + MASK_BYTES;
     // barriers: q_full[NQ] full[NS] empty[NS] s_full[NQ] p_full[NQ] o_full[NQ] done
     static constexpr int BAR_QFULL = 0;
     static constexpr int BAR_FULL = BAR_QFULL + NQ;
@@ -114,11 +117,11 @@ struct TcParams {
 };
 
 template <int D, int BR, int BC, int NQ, bool MASKED>
-__global__ void __launch_bounds__(TcShape<D, BR, BC, NQ>::THREADS, 1)
+__global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                        const TcParams p) {
-    using S = TcShape<D, BR, BC, NQ>;
+    using S = TcShape<D, BR, BC, NQ, MASKED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -179,32 +182,43 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ>::THREADS, 1)
 
     if (warp >= S::SOFTMAX_WARPS) {
         if constexpr (S::SPLIT_REGS) regs_dec<S::REGS_OTHER>();
+        // The producer and MMA warps run their loops on all 32 lanes with
+        // warp-uniform values (so address and descriptor arithmetic stays on
+        // the uniform datapath) and one elected lane issues each copy, MMA
+        // and commit.  A wait counts as failed for the warp if any lane's
+        // bounded wait gave up, so every lane leaves a loop together.
+        auto wwait = [&](uint32_t b, uint32_t parity, int site) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(b, parity, abort_flag, p.err, site));
+        };
+        const bool leader = elect_one();
         if (warp == S::WARP_TMA) {
             // --------------------------------------------------------------
             // TMA producer
             // --------------------------------------------------------------
-            if (lane == 0) {
+            if (leader) {
                 tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(&tm_k);
                 tma_prefetch_desc(&tm_v);
                 tma_prefetch_desc(&tm_o);
-                const uint64_t pol_kv = l2_policy_evict_last();   // K/V are re-read by every query group
-                const uint64_t pol_q = l2_policy_evict_first();   // Q is read once
-                for (int q = 0; q < NQ; ++q) {
-                    if (nkv[q] == 0) continue;
+            }
+            const uint64_t pol_kv = l2_policy_evict_last();   // K/V are re-read by every query group
+            const uint64_t pol_q = l2_policy_evict_first();   // Q is read once
+            for (int q = 0; q < NQ; ++q) {
+                if (nkv[q] == 0) continue;
+                if (leader) {
                     mbar_arrive_expect_tx(bar(S::BAR_QFULL + q), S::Q_BYTES);
 #pragma unroll
                     for (int cb = 0; cb < S::CB; ++cb)
                         tma_load_3d_hint(sQ + q * S::Q_BYTES + cb * (BR * 128), &tm_q, bar(S::BAR_QFULL + q),
                                          cb * 64, r0[q], bh, pol_q);
                 }
-                const int T = 2 * nkv_max;  // K_0 V_0 K_1 V_1 ...
-                int issued = 0;
-                for (int t = 0; t < T; ++t) {
-                    const int slot = t % S::NS, round = t / S::NS;
-                    if (round > 0 &&
-                        !mbar_wait(bar(S::BAR_EMPTY + slot), (round - 1) & 1, abort_flag, p.err, 1))
-                        break;
+            }
+            const int T = 2 * nkv_max;  // K_0 V_0 K_1 V_1 ...
+            int issued = 0;
+            for (int t = 0; t < T; ++t) {
+                const int slot = t % S::NS, round = t / S::NS;
+                if (round > 0 && !wwait(bar(S::BAR_EMPTY + slot), (round - 1) & 1, 1)) break;
+                if (leader) {
                     mbar_arrive_expect_tx(bar(S::BAR_FULL + slot), S::SLOT_BYTES);
                     const CUtensorMap *m = (t & 1) ? &tm_v : &tm_k;
                     const int j = t >> 1;
@@ -212,93 +226,102 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ>::THREADS, 1)
                     for (int cb = 0; cb < S::CB; ++cb)
                         tma_load_3d_hint(sRing + slot * S::SLOT_BYTES + cb * (BC * 128), m,
                                          bar(S::BAR_FULL + slot), cb * 64, j * BC, bh, pol_kv);
-                    issued = t + 1;
                 }
-                // Drain: every copy this thread started has landed before the
-                // CTA may exit (normally already true).
-                for (int t = max(0, issued - S::NS); t < issued; ++t)
-                    mbar_wait(bar(S::BAR_FULL + t % S::NS), (t / S::NS) & 1, abort_flag, p.err, 2);
-                for (int q = 0; q < NQ; ++q)
-                    if (nkv[q] > 0) mbar_wait(bar(S::BAR_QFULL + q), 0, abort_flag, p.err, 3);
+                issued = t + 1;
             }
+            // Drain: every copy this warp started has landed before the CTA
+            // may exit (normally already true).
+            for (int t = max(0, issued - S::NS); t < issued; ++t)
+                wwait(bar(S::BAR_FULL + t % S::NS), (t / S::NS) & 1, 2);
+            for (int q = 0; q < NQ; ++q)
+                if (nkv[q] > 0) wwait(bar(S::BAR_QFULL + q), 0, 3);
             __syncwarp();
         } else if (warp == S::WARP_MMA) {
             // --------------------------------------------------------------
-            // MMA issuer (one thread)
+            // MMA issuer (one elected lane)
             // --------------------------------------------------------------
-            if (lane == 0) {
-                constexpr uint32_t idesc_s = idesc_bf16_f32(BR, BC, false, false);  // Q, K both K-major
-                constexpr uint32_t idesc_o = idesc_bf16_f32(BR, D, false, true);    // P (TMEM), V MN-major
-                bool ok = true;
-                for (int q = 0; q < NQ && ok; ++q)
-                    if (nkv[q] > 0) ok = mbar_wait(bar(S::BAR_QFULL + q), 0, abort_flag, p.err, 10);
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BR, BC, false, false);  // Q, K both K-major
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BR, D, false, true);    // P (TMEM), V MN-major
+            bool ok = true;
+            for (int q = 0; q < NQ && ok; ++q)
+                if (nkv[q] > 0) ok = wwait(bar(S::BAR_QFULL + q), 0, 10);
 
-                auto issue_s = [&](int q, int j) {
-                    const uint32_t kslot = sRing + ((2 * j) % S::NS) * S::SLOT_BYTES;
-                    const uint32_t qbuf = sQ + q * S::Q_BYTES;
+            // Descriptors differ only in their start-address field (bits
+            // 0..13, address >> 4): build one base per operand and add.
+            const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
+            const uint64_t kdesc0 = sdesc_sw128(sRing, 16, 1024);
+            const uint64_t vdesc0 = sdesc_sw128(sRing, BC * 128, 1024);
+            auto issue_s = [&](int q, int j) {
+                const uint64_t a0 = qdesc0 + static_cast<uint64_t>((q * S::Q_BYTES) >> 4);
+                const uint64_t b0 = kdesc0 + static_cast<uint64_t>((((2 * j) % S::NS) * S::SLOT_BYTES) >> 4);
+                if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int cb = kk >> 2, off = (kk & 3) * 32;
-                        const uint64_t a = sdesc_sw128(qbuf + cb * (BR * 128) + off, 16, 1024);
-                        const uint64_t b = sdesc_sw128(kslot + cb * (BC * 128) + off, 16, 1024);
-                        mma_bf16_ss(tmem + S::s_col(q), a, b, idesc_s, kk > 0 ? 1u : 0u);
+                        mma_bf16_ss(tmem + S::s_col(q), a0 + static_cast<uint64_t>((cb * (BR * 128) + off) >> 4),
+                                    b0 + static_cast<uint64_t>((cb * (BC * 128) + off) >> 4), idesc_s,
+                                    kk > 0 ? 1u : 0u);
                     }
                     tc_commit(bar(S::BAR_SFULL + q));
-                };
-                auto issue_pv = [&](int q, int j) {
-                    const uint32_t vslot = sRing + ((2 * j + 1) % S::NS) * S::SLOT_BYTES;
+                }
+            };
+            auto issue_pv = [&](int q, int j) {
+                const uint64_t b0 = vdesc0 + static_cast<uint64_t>((((2 * j + 1) % S::NS) * S::SLOT_BYTES) >> 4);
+                if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < BC / 16; ++kk) {
-                        const uint64_t b = sdesc_sw128(vslot + kk * 2048, BC * 128, 1024);
-                        mma_bf16_ts(tmem + S::o_col(q), tmem + S::s_col(q) + kk * 8, b, idesc_o,
+                        mma_bf16_ts(tmem + S::o_col(q), tmem + S::s_col(q) + kk * 8,
+                                    b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_o,
                                     (j > 0 || kk > 0) ? 1u : 0u);
                     }
-                };
+                }
+            };
+            auto commit = [&](int b) {
+                if (leader) tc_commit(bar(b));
+            };
 
-                if (ok && nkv_max > 0) {
-                    ok = mbar_wait(bar(S::BAR_FULL + 0), 0, abort_flag, p.err, 11);  // K_0
-                    if (ok) {
-                        tc_fence_after();
-                        for (int q = 0; q < NQ; ++q)
-                            if (nkv[q] > 0) issue_s(q, 0);
-                        tc_commit(bar(S::BAR_EMPTY + 0));
-                    }
-                }
-                for (int j = 0; ok && j < nkv_max; ++j) {
-                    const int tv = 2 * j + 1;
-                    if (!mbar_wait(bar(S::BAR_FULL + tv % S::NS), (tv / S::NS) & 1, abort_flag, p.err, 12)) break;
+            if (ok && nkv_max > 0) {
+                ok = wwait(bar(S::BAR_FULL + 0), 0, 11);  // K_0
+                if (ok) {
                     tc_fence_after();
-                    bool k_ready = false;
-                    const int tk = 2 * j + 2;
-                    for (int q = 0; q < NQ && ok; ++q) {
-                        if (j >= nkv[q]) continue;
-                        if (!mbar_wait(bar(S::BAR_PFULL + q), j & 1, abort_flag, p.err, 13)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_pv(q, j);
-                        if (j == nkv[q] - 1) tc_commit(bar(S::BAR_OFULL + q));
-                        if (j + 1 < nkv[q]) {
-                            if (!k_ready) {
-                                if (!mbar_wait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, abort_flag, p.err,
-                                               14)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                                k_ready = true;
-                            }
-                            issue_s(q, j + 1);
-                        }
-                    }
-                    tc_commit(bar(S::BAR_EMPTY + tv % S::NS));               // V_j slot
-                    if (k_ready) tc_commit(bar(S::BAR_EMPTY + tk % S::NS));  // K_{j+1} slot
+                    for (int q = 0; q < NQ; ++q)
+                        if (nkv[q] > 0) issue_s(q, 0);
+                    commit(S::BAR_EMPTY + 0);
                 }
-                // Every MMA issued has completed before tensor memory is released.
-                tc_commit(bar(S::BAR_DONE));
-                mbar_wait(bar(S::BAR_DONE), 0, abort_flag, p.err, 15);
             }
+            for (int j = 0; ok && j < nkv_max; ++j) {
+                const int tv = 2 * j + 1;
+                if (!wwait(bar(S::BAR_FULL + tv % S::NS), (tv / S::NS) & 1, 12)) break;
+                tc_fence_after();
+                bool k_ready = false;
+                const int tk = 2 * j + 2;
+                for (int q = 0; q < NQ && ok; ++q) {
+                    if (j >= nkv[q]) continue;
+                    if (!wwait(bar(S::BAR_PFULL + q), j & 1, 13)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(q, j);
+                    if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
+                    if (j + 1 < nkv[q]) {
+                        if (!k_ready) {
+                            if (!wwait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, 14)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            k_ready = true;
+                        }
+                        issue_s(q, j + 1);
+                    }
+                }
+                commit(S::BAR_EMPTY + tv % S::NS);               // V_j slot
+                if (k_ready) commit(S::BAR_EMPTY + tk % S::NS);  // K_{j+1} slot
+            }
+            // Every MMA issued has completed before tensor memory is released.
+            commit(S::BAR_DONE);
+            wwait(bar(S::BAR_DONE), 0, 15);
             __syncwarp();
         }
     } else {
@@ -331,16 +354,33 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ>::THREADS, 1)
             // diagonal, or any tile when a key mask is given.
             const bool edge = MASKED || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0[q]);
 
+            const bool diag = p.causal && key0 + BC - 1 > r0[q];   // tile crosses the causal diagonal
+            // Key mask of this tile, once per warpgroup, in log2 units with -inf
+            // past N; double-buffered so one barrier per tile suffices.
+            const float *msm = reinterpret_cast<const float *>(smem + S::OFF_MASK) + (q * 2 + (j & 1)) * BC;
+            if constexpr (MASKED) {
+                float *mw = reinterpret_cast<float *>(smem + S::OFF_MASK) + (q * 2 + (j & 1)) * BC;
+#pragma unroll
+                for (int t = row_in; t < BC; t += 128) {
+                    const int key = key0 + t;
+                    mw[t] = (key < N) ? __ldg(mrow + key) * kLog2e : kNegInf;
+                }
+                named_bar_sync(3 + q, 128);
+            }
             // One loaded 32-column chunk -> log2-domain scores
             // x = s*scale*log2(e) (+ mask*log2(e)), -inf where not allowed.
             auto mask_chunk = [&](int c, uint32_t *r) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int key = key0 + 32 * c + e;
-                    float x = __uint_as_float(r[e]) * sl2;
-                    if (MASKED) x = (key < N) ? fmaf(__ldg(mrow + key), kLog2e, x) : kNegInf;
-                    const bool allowed = (key < N) && (!p.causal || key <= row);
-                    r[e] = __float_as_uint(allowed ? x : kNegInf);
+                    float x;
+                    if constexpr (MASKED) {
+                        x = fmaf(__uint_as_float(r[e]), sl2, msm[32 * c + e]);
+                    } else {
+                        x = (key < N) ? __uint_as_float(r[e]) * sl2 : kNegInf;
+                    }
+                    if (diag) x = (key <= row) ? x : kNegInf;
+                    r[e] = __float_as_uint(x);
                 }
             };
             auto chunk_max = [&](const uint32_t *r, float mx) {
@@ -351,6 +391,8 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ>::THREADS, 1)
             // p = 2^(x - m_use) for one chunk, packed to bf16 pairs and written
             // over S's first BC/2 columns (chunk c -> columns 16c .. 16c+15,
             // never ahead of the chunks still to be read).
+            // Partial sums per chunk keep the add chains short: ls2 sums the
+            // float32 p, lr2 the bf16-rounded p (both as float32 pairs).
             auto exp_chunk = [&](int c, const uint32_t *r, uint64_t negm2, uint64_t &ls2, uint64_t &lr2) {
                 const uint64_t sl2x2 = f2_pack(sl2, sl2);
                 uint32_t pk[16];
@@ -370,44 +412,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ>::THREADS, 1)
                 tmem_st16(tS + 16 * c, pk);
             };
 
-            constexpr bool kTwoPass = BC > 128;   // 256 columns do not fit in registers
-            constexpr int kRegCols = kTwoPass ? 32 : BC;
-            uint32_t sr[kRegCols];
-            float mx = kNegInf;
-            if constexpr (!kTwoPass) {
-#pragma unroll
-                for (int c = 0; c < BC / 32; ++c) tmem_ld32(tS + 32 * c, sr + 32 * c);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < BC / 32; ++c) reg_fence32(sr + 32 * c);
-                if (edge) {
-#pragma unroll
-                    for (int c = 0; c < BC / 32; ++c) {
-                        mask_chunk(c, sr + 32 * c);
-                        mx = chunk_max(sr + 32 * c, mx);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < BC / 32; ++c) mx = chunk_max(sr + 32 * c, mx);
-                    mx *= sl2;   // scale > 0: max commutes with the scaling
-                }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < BC / 32; ++c) {
-                    tmem_ld32(tS + 32 * c, sr);
-                    tmem_ld_wait();
-                    reg_fence32(sr);
-                    if (edge) mask_chunk(c, sr);
-                    mx = chunk_max(sr, mx);
-                }
-                if (!edge) mx *= sl2;
-            }
-
-            const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
-            const bool moved = (m_new != m);
-            const float alpha = moved ? ex2(m - m_new) : 1.f;
-            const float m_use = (m_new == kNegInf) ? 0.f : m_new;
-            if (j > 0 && __any_sync(0xffffffffu, moved)) {
+            // O_q *= alpha for this warp's rows (warp-collective; alpha = 1 for
+            // rows whose reference did not move).
+            auto rescale_o = [&](float alpha) {
                 const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -425,29 +432,131 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ>::THREADS, 1)
                     }
                     tmem_st32(tO + 32 * c, o);
                 }
-            }
-            m = m_new;
+            };
 
-            const uint64_t negm2 = f2_pack(-m_use, -m_use);
-            uint64_t ls2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
+            constexpr bool kTwoPass = BC > 128;   // 256 columns do not fit in registers
+            float tile_ls = 0.f, tile_lr = 0.f;
+            float alpha = 1.f;
             if constexpr (!kTwoPass) {
+                uint32_t sr[BC];
+                uint32_t pk[BC / 2];
+                auto load_tile = [&]() {
 #pragma unroll
-                for (int c = 0; c < BC / 32; ++c) exp_chunk(c, sr + 32 * c, negm2, ls2, lr2);
+                    for (int c = 0; c < BC / 32; ++c) tmem_ld32(tS + 32 * c, sr + 32 * c);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < BC / 32; ++c) reg_fence32(sr + 32 * c);
+                    if (edge) {
+#pragma unroll
+                        for (int c = 0; c < BC / 32; ++c) mask_chunk(c, sr + 32 * c);
+                    }
+                };
+                // p = 2^(x - m_use) for the whole tile into pk (bf16 pairs) and
+                // the two tile sums; with want_max also the tile maximum of x
+                // (log2 units), computed alongside instead of before.
+                auto exps = [&](float m_use, bool want_max) -> float {
+                    const uint64_t negm2 = f2_pack(-m_use, -m_use);
+                    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                    float mx = kNegInf;
+                    tile_ls = 0.f;
+                    tile_lr = 0.f;
+#pragma unroll
+                    for (int c = 0; c < BC / 32; ++c) {
+                        uint64_t ls2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
+                        float cmx = kNegInf;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float x0 = __uint_as_float(sr[32 * c + 2 * e]);
+                            const float x1 = __uint_as_float(sr[32 * c + 2 * e + 1]);
+                            if (want_max) cmx = fmax3(cmx, x0, x1);
+                            const uint64_t xx = f2_pack(x0, x1);
+                            const uint64_t y = edge ? f2_add(xx, negm2) : f2_fma(xx, sl2x2, negm2);
+                            float y0, y1;
+                            f2_unpack(y, y0, y1);
+                            const float p0 = ex2(y0), p1 = ex2(y1);
+                            uint32_t w = pack_bf16x2(p0, p1);
+                            if (!active) w = 0u;
+                            pk[16 * c + e] = w;
+                            ls2 = f2_add(ls2, f2_pack(p0, p1));
+                            lr2 = f2_add(lr2, f2_pack(bf16lo_to_f32(w), bf16hi_to_f32(w)));
+                        }
+                        float s0, s1, t0, t1;
+                        f2_unpack(ls2, s0, s1);
+                        f2_unpack(lr2, t0, t1);
+                        tile_ls += s0 + s1;
+                        tile_lr += t0 + t1;
+                        mx = fmaxf(mx, cmx);
+                    }
+                    return edge ? mx : mx * sl2;   // scale > 0: max commutes with the scaling
+                };
+                load_tile();
+                if (__all_sync(0xffffffffu, !active || m != kNegInf)) {
+                    // Every row has a finite reference: one pass against it, the
+                    // tile maximum computed alongside.  Only if some row's
+                    // maximum jumps past the threshold is the tile redone (S is
+                    // still intact in tensor memory; P is written below).
+                    const float mx = exps(m, true);
+                    const bool need = active && (mx > m + kRescaleThresh);
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float m_new = need ? mx : m;
+                        alpha = need ? ex2(m - m_new) : 1.f;
+                        rescale_o(alpha);   // j > 0 here: a finite reference needs an earlier tile
+                        m = m_new;
+                        load_tile();
+                        exps(m, false);
+                    }
+                } else {
+                    // Maximum first: a row's first tile, or rows with no allowed
+                    // key so far.
+                    float mx = kNegInf;
+#pragma unroll
+                    for (int c = 0; c < BC / 32; ++c) mx = chunk_max(sr + 32 * c, mx);
+                    if (!edge) mx *= sl2;
+                    const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
+                    const bool moved = (m_new != m);
+                    alpha = moved ? ex2(m - m_new) : 1.f;
+                    if (j > 0 && __any_sync(0xffffffffu, moved)) rescale_o(alpha);
+                    m = m_new;
+                    exps(m == kNegInf ? 0.f : m, false);
+                }
+#pragma unroll
+                for (int c = 0; c < BC / 32; ++c) tmem_st16(tS + 16 * c, pk + 16 * c);
             } else {
+                uint32_t sr[32];
+                float mx = kNegInf;
 #pragma unroll 1
                 for (int c = 0; c < BC / 32; ++c) {
                     tmem_ld32(tS + 32 * c, sr);
                     tmem_ld_wait();
                     reg_fence32(sr);
                     if (edge) mask_chunk(c, sr);
+                    mx = chunk_max(sr, mx);
+                }
+                if (!edge) mx *= sl2;
+                const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
+                const bool moved = (m_new != m);
+                alpha = moved ? ex2(m - m_new) : 1.f;
+                const float m_use = (m_new == kNegInf) ? 0.f : m_new;
+                if (j > 0 && __any_sync(0xffffffffu, moved)) rescale_o(alpha);
+                m = m_new;
+                const uint64_t negm2 = f2_pack(-m_use, -m_use);
+#pragma unroll 1
+                for (int c = 0; c < BC / 32; ++c) {
+                    tmem_ld32(tS + 32 * c, sr);
+                    tmem_ld_wait();
+                    reg_fence32(sr);
+                    if (edge) mask_chunk(c, sr);
+                    uint64_t ls2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
                     exp_chunk(c, sr, negm2, ls2, lr2);
+                    float s0, s1, t0, t1;
+                    f2_unpack(ls2, s0, s1);
+                    f2_unpack(lr2, t0, t1);
+                    tile_ls += s0 + s1;
+                    tile_lr += t0 + t1;
                 }
             }
-            float s0, s1, t0, t1;
-            f2_unpack(ls2, s0, s1);
-            f2_unpack(lr2, t0, t1);
-            l_exact = l_exact * alpha + (s0 + s1);
-            l_round = l_round * alpha + (t0 + t1);
+            l_exact = l_exact * alpha + tile_ls;
+            l_round = l_round * alpha + tile_lr;
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(S::BAR_PFULL + q));
@@ -527,7 +636,7 @@ bool make_map(CUtensorMap *m, const void *base, int D, int N, int BH, int box_ro
 template <int D, int BR, int BC, int NQ, bool MASKED>
 int launch_variant(const void *Q, const void *K, const void *V, void *O, float *LSE, int BH, int N,
                    int causal, float scale, const float *key_mask, cudaStream_t stream) {
-    using S = TcShape<D, BR, BC, NQ>;
+    using S = TcShape<D, BR, BC, NQ, MASKED>;
     auto kern = attn_fwd_tc_kernel<D, BR, BC, NQ, MASKED>;
     static int attr_device = -1;
     int dev = 0;

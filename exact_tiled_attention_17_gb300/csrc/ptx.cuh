@@ -55,6 +55,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// As above, but the thread may stay suspended in the instruction for up to
+// `hint_ns` while the phase is incomplete (it resumes as soon as it completes),
+// so a waiting warp issues far fewer polling instructions.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns`, or as soon as *abort is non-zero (another thread of the CTA
@@ -65,17 +79,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
-                atomicOr(err, kErrTimeout | (site << 8));
-                *abort = 1u;
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity, 100000u)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(err, kErrTimeout | (site << 8));
+            *abort = 1u;
+            return false;
         }
     }
+}
+
+// One lane of the (converged) warp returns true.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t.reg .b32 R;\n\t"
+        "elect.sync R|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32).
