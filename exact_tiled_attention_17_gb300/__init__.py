@@ -32,7 +32,9 @@ ATTN_ERR_DEVICE_TIMEOUT = -5
 
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_naive_workspace_size", "attn_naive_fwd", "attn_deviation_workspace_size",
-           "attn_deviation", "attn_status", "attn_strerror", "attn_last_variant", "attn_debug_wait_timeout")
+           "attn_deviation", "attn_deviation_noalloc", "attn_status", "attn_strerror", "attn_last_variant",
+           "attn_debug_wait_timeout")
+DEVIATION_NOALLOC_MAX_N = 1 << 20
 
 _DTYPE = {torch.float32: ATTN_F32, torch.bfloat16: ATTN_BF16, torch.float64: ATTN_F64}
 
@@ -64,6 +66,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_deviation_workspace_size.restype = sz
     lib.attn_deviation.argtypes = [vp, i, vp, i, ll, vp, sz, vp, ctypes.POINTER(DevT)]
     lib.attn_deviation.restype = i
+    lib.attn_deviation_noalloc.argtypes = [vp, i, vp, i, ll, vp, ctypes.POINTER(DevT)]
+    lib.attn_deviation_noalloc.restype = i
     lib.attn_status.argtypes = [vp]
     lib.attn_status.restype = i
     lib.attn_strerror.argtypes = [i]
@@ -191,6 +195,22 @@ def attn_deviation(a, b, workspace=None, stream=None) -> dict:
     rc = lib.attn_deviation(_ptr(a), _DTYPE[a.dtype], _ptr(b), _DTYPE[b.dtype], n, _ptr(ws), ws.numel(),
                             ctypes.c_void_p(_stream(stream)), ctypes.byref(res))
     _check(rc, "attn_deviation")
+    return {"max_abs": res.max_abs, "w1": res.w1, "mean_abs": res.mean_abs, "std_abs": res.std_abs,
+            "mean_signed": res.mean_signed, "n": res.n}
+
+
+def attn_deviation_noalloc(a, b, stream=None) -> dict:
+    """attn_deviation without a workspace, for callers that cannot allocate
+    device memory (the library's own fixed scratch array is used instead;
+    n <= DEVIATION_NOALLOC_MAX_N; calls that overlap on the GPU race)."""
+    if a.numel() != b.numel():
+        raise ValueError("a and b must have the same number of elements")
+    a = a.contiguous()
+    b = b.contiguous()
+    res = DevT()
+    rc = lib.attn_deviation_noalloc(_ptr(a), _DTYPE[a.dtype], _ptr(b), _DTYPE[b.dtype], a.numel(),
+                                    ctypes.c_void_p(_stream(stream)), ctypes.byref(res))
+    _check(rc, "attn_deviation_noalloc")
     return {"max_abs": res.max_abs, "w1": res.w1, "mean_abs": res.mean_abs, "std_abs": res.std_abs,
             "mean_signed": res.mean_signed, "n": res.n}
 

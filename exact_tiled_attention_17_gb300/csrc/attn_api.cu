@@ -179,6 +179,25 @@ int attn_deviation(const void *a, int ta, const void *b, int tb, long long n, vo
     return kOk;
 }
 
+static_assert(ATTN_DEVIATION_NOALLOC_MAX_N == eta::kDeviationNoAllocMaxN, "header and library agree on the limit");
+
+int attn_deviation_noalloc(const void *a, int ta, const void *b, int tb, long long n, void *stream,
+                           attn_dev_t *out) {
+    if (!a || !b || !out || n <= 0) return kErrArg;
+    if (ta < ATTN_F32 || ta > ATTN_F64 || tb < ATTN_F32 || tb > ATTN_F64) return kErrArg;
+    if (n > ATTN_DEVIATION_NOALLOC_MAX_N) return kErrUnsupported;
+    double host[5];
+    const int rc = launch_deviation_noalloc(a, ta, b, tb, n, static_cast<cudaStream_t>(stream), host);
+    if (rc != kOk) return rc;
+    out->max_abs = host[0];
+    out->w1 = host[1];
+    out->mean_abs = host[2];
+    out->std_abs = host[3];
+    out->mean_signed = host[4];
+    out->n = n;
+    return kOk;
+}
+
 int attn_status(void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(st) != cudaSuccess) return kErrCuda;

@@ -10,6 +10,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 
@@ -23,15 +24,15 @@ constexpr int kRedBlocks = 1024;
 constexpr int kRedThreads = 256;
 constexpr int kScanChunk = 1024;
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
     size_t keys_a, keys_b, tmp, hist, chunk_sums, part, result, total;
     long long nb, hist_len, nchunks;
 };
 
-Layout layout(long long n) {
-    Layout L;
+constexpr Layout layout(long long n) {
+    Layout L{};
     L.nb = (n + kTile - 1) / kTile;
     L.hist_len = 256 * L.nb;
     L.nchunks = (L.hist_len + kScanChunk - 1) / kScanChunk;
@@ -337,6 +338,46 @@ int radix_sort(uint64_t *keys, uint64_t *tmp, long long n, const Layout &L, char
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry: the same kernels with their scratch in a file-scope
+// device array instead of a caller workspace.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocBytes = layout(kDeviationNoAllocMaxN).total;
+static __device__ __align__(256) unsigned char g_deviation_scratch[kNoAllocBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64];   // device address of g_deviation_scratch, per device
+}  // namespace
+
+int launch_deviation_noalloc(const void *a, int ta, const void *b, int tb, long long n, cudaStream_t stream,
+                             double *host_result) {
+    if (n > kDeviationNoAllocMaxN) return kErrUnsupported;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kErrCuda;
+    void *ws = nullptr;
+    {
+        // Set-up, once per device, with that device current: the host-side
+        // name of the array is only a stand-in, so ask the runtime for its
+        // device address.
+        std::lock_guard<std::mutex> lk(g_scratch_mu);
+        if (!g_scratch_ptr[dev]) {
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_deviation_scratch) != cudaSuccess || ptr == nullptr) return kErrCuda;
+            g_scratch_ptr[dev] = ptr;
+        }
+        ws = g_scratch_ptr[dev];
+    }
+    // Every scratch word the kernels read is written earlier in the same call
+    // (keys, histograms, scans, partial sums, result), so nothing needs clearing.
+    double *dev_result = reinterpret_cast<double *>(static_cast<char *>(ws) + layout(n).result);
+    const int rc = launch_deviation(a, ta, b, tb, n, ws, stream, dev_result);
+    if (rc != kOk) return rc;
+    if (cudaMemcpyAsync(host_result, dev_result, 5 * sizeof(double), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return kErrCuda;
+    return cudaStreamSynchronize(stream) == cudaSuccess ? kOk : kErrCuda;
+}
 
 size_t deviation_workspace_bytes(long long n) { return layout(n).total; }
 size_t deviation_result_offset(long long n) { return layout(n).result; }

@@ -47,6 +47,11 @@ int launch_deviation(const void *a, int ta, const void *b, int tb, long long n, 
                      cudaStream_t stream, double *dev_result /* 5 doubles inside workspace */);
 size_t deviation_result_offset(long long n);
 
+// Allocation-free deviation (scratch in a static device array of deviation.cu).
+constexpr long long kDeviationNoAllocMaxN = 1LL << 20;
+int launch_deviation_noalloc(const void *a, int ta, const void *b, int tb, long long n, cudaStream_t stream,
+                             double *host_result /* 5 doubles */);
+
 // Bounded-wait self-test kernel (attn_api.cu).
 int launch_wait_timeout_probe(unsigned timeout_us, cudaStream_t stream);
 

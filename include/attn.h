@@ -133,6 +133,29 @@ int attn_deviation(const void *a, int ta, const void *b, int tb, long long n,
                    void *workspace, size_t ws_bytes, void *stream, attn_dev_t *out);
 
 /*
+ * attn_deviation_noalloc — the same measures as attn_deviation for callers
+ * that cannot allocate device memory: for example a plain C host program
+ * with no device allocator of its own, or a process whose device memory is
+ * already reserved up front by another framework's caching pool, where a
+ * cudaMalloc for a workspace would fail or break that pool's accounting.
+ * (The paper has no counterpart: this is a convenience of the library.)
+ *
+ * Instead of a caller workspace it uses one scratch array that the library
+ * keeps in device memory for the life of the process on every GPU that loads
+ * it: about 24 MiB, enough for n <= ATTN_DEVIATION_NOALLOC_MAX_N elements.
+ * Larger n returns ATTN_ERR_UNSUPPORTED (use attn_deviation with a workspace).
+ * It calls no cudaMalloc or cudaFree.  The first call on a device looks up
+ * the array's device address on that device; make that first call before
+ * any stream capture begins.  All calls share the one array, so calls that
+ * can overlap on the GPU (different streams or threads at the same time)
+ * race with each other and must be serialised by the caller.  Arguments and
+ * result as for attn_deviation; synchronous.
+ */
+#define ATTN_DEVIATION_NOALLOC_MAX_N 1048576LL
+int attn_deviation_noalloc(const void *a, int ta, const void *b, int tb, long long n, void *stream,
+                           attn_dev_t *out);
+
+/*
  * attn_status — waits for `stream`, then returns ATTN_ERR_DEVICE_TIMEOUT if a
  * kernel of this library recorded a timed-out wait since the last call
  * (and clears the record), ATTN_ERR_CUDA if the stream reports a CUDA error,
