@@ -29,9 +29,12 @@
 // BR = 64 uses M = 64 MMAs, whose accumulator rows r sit in tensor-memory lane
 // 32*(r/16) + r%16: lanes 0..15 of each warp carry rows, lanes 16..31 idle.
 //
-// The reference maximum is moved only when the tile maximum exceeds it by
-// more than kRescaleThresh (log2 units): exact up to rounding because a / l
-// does not depend on the reference point, and p = 2^(x - m) stays <= 2^8.
+// The reference maximum m is set from a row's first tile with an allowed key
+// (moved only if the tile maximum exceeds it by more than kRescaleThresh, log2
+// units).  Later tiles are exponentiated against m without computing their
+// maximum; only a tile whose p sum past kFastSumLimit = 2^16 moves m to its
+// maximum and is redone.  Exact up to rounding because a / l does not depend
+// on the reference point, and every p stays <= 2^16.
 // Two denominators are kept: the sum of the bf16-rounded p that actually
 // enter P V (normalises O, so the applied weights sum to one) and the float32
 // sum of p (gives the LSE).
@@ -47,6 +50,9 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThresh = 8.0f;
+// A tile whose p = 2^(x - m) sum to at most this needs no move of the
+// reference maximum: every p is at most the sum.
+constexpr float kFastSumLimit = 65536.0f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
 template <int D, int BR, int BC, int NQ, bool MASKED>
@@ -452,23 +458,19 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                     }
                 };
                 // p = 2^(x - m_use) for the whole tile into pk (bf16 pairs) and
-                // the two tile sums; with want_max also the tile maximum of x
-                // (log2 units), computed alongside instead of before.
-                auto exps = [&](float m_use, bool want_max) -> float {
+                // the two tile sums.
+                auto exps = [&](float m_use) {
                     const uint64_t negm2 = f2_pack(-m_use, -m_use);
                     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-                    float mx = kNegInf;
                     tile_ls = 0.f;
                     tile_lr = 0.f;
 #pragma unroll
                     for (int c = 0; c < BC / 32; ++c) {
                         uint64_t ls2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
-                        float cmx = kNegInf;
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const float x0 = __uint_as_float(sr[32 * c + 2 * e]);
                             const float x1 = __uint_as_float(sr[32 * c + 2 * e + 1]);
-                            if (want_max) cmx = fmax3(cmx, x0, x1);
                             const uint64_t xx = f2_pack(x0, x1);
                             const uint64_t y = edge ? f2_add(xx, negm2) : f2_fma(xx, sl2x2, negm2);
                             float y0, y1;
@@ -485,42 +487,52 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                         f2_unpack(lr2, t0, t1);
                         tile_ls += s0 + s1;
                         tile_lr += t0 + t1;
-                        mx = fmaxf(mx, cmx);
                     }
+                };
+                auto store_p = [&]() {
+#pragma unroll
+                    for (int c = 0; c < BC / 32; ++c) tmem_st16(tS + 16 * c, pk + 16 * c);
+                };
+                auto tile_max = [&]() {
+                    float mx = kNegInf;
+#pragma unroll
+                    for (int c = 0; c < BC / 32; ++c) mx = chunk_max(sr + 32 * c, mx);
                     return edge ? mx : mx * sl2;   // scale > 0: max commutes with the scaling
                 };
                 load_tile();
                 if (__all_sync(0xffffffffu, !active || m != kNegInf)) {
-                    // Every row has a finite reference: one pass against it, the
-                    // tile maximum computed alongside.  Only if some row's
-                    // maximum jumps past the threshold is the tile redone (S is
-                    // still intact in tensor memory; P is written below).
-                    const float mx = exps(m, true);
-                    const bool need = active && (mx > m + kRescaleThresh);
-                    if (__any_sync(0xffffffffu, need)) {
-                        const float m_new = need ? mx : m;
+                    // Every row has a finite reference: exponentiate against it
+                    // in one pass, with no maximum.  A row whose tile sum
+                    // exceeds kFastSumLimit (or overflows) has a score far past
+                    // the reference: only then is the tile's maximum taken and
+                    // the tile redone (S is still intact in tensor memory; P is
+                    // written below).
+                    exps(m);
+                    const bool need = active && !(tile_ls <= kFastSumLimit);
+                    if (!__any_sync(0xffffffffu, need)) {
+                        store_p();
+                    } else {
+                        load_tile();
+                        const float mx = tile_max();
+                        const float m_new = need ? fmaxf(mx, m) : m;
                         alpha = need ? ex2(m - m_new) : 1.f;
                         rescale_o(alpha);   // j > 0 here: a finite reference needs an earlier tile
                         m = m_new;
-                        load_tile();
-                        exps(m, false);
+                        exps(m);
+                        store_p();
                     }
                 } else {
                     // Maximum first: a row's first tile, or rows with no allowed
                     // key so far.
-                    float mx = kNegInf;
-#pragma unroll
-                    for (int c = 0; c < BC / 32; ++c) mx = chunk_max(sr + 32 * c, mx);
-                    if (!edge) mx *= sl2;
+                    const float mx = tile_max();
                     const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
                     const bool moved = (m_new != m);
                     alpha = moved ? ex2(m - m_new) : 1.f;
                     if (j > 0 && __any_sync(0xffffffffu, moved)) rescale_o(alpha);
                     m = m_new;
-                    exps(m == kNegInf ? 0.f : m, false);
+                    exps(m == kNegInf ? 0.f : m);
+                    store_p();
                 }
-#pragma unroll
-                for (int c = 0; c < BC / 32; ++c) tmem_st16(tS + 16 * c, pk + 16 * c);
             } else {
                 uint32_t sr[32];
                 float mx = kNegInf;
