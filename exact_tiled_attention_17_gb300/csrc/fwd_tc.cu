@@ -85,7 +85,7 @@ struct TcShape {
     static constexpr int OFF_RING = NQ * Q_BYTES;
     static constexpr int OFF_MASK = OFF_RING + NS * SLOT_BYTES;
     static constexpr int OFF_BAR = OFF_MASK + MASK_BYTES;
-    // barriers: q_full[NQ] full[NS] empty[NS] s_full[NQ] p_full[NQ] o_full[NQ] done
+    // barriers: q_full[NQ] full[NS] empty[NS] s_full[NQ] p_full[NQ] o_full[NQ] done part done_read
     static constexpr int BAR_QFULL = 0;
     static constexpr int BAR_FULL = BAR_QFULL + NQ;
     static constexpr int BAR_EMPTY = BAR_FULL + NS;
@@ -93,7 +93,13 @@ struct TcShape {
     static constexpr int BAR_PFULL = BAR_SFULL + NQ;
     static constexpr int BAR_OFULL = BAR_PFULL + NQ;
     static constexpr int BAR_DONE = BAR_OFULL + NQ;
-    static constexpr int NBARS = BAR_DONE + 1;
+    static constexpr int BAR_PART = BAR_DONE + 1;       // split K/V: partials of the other parts are ready
+    static constexpr int BAR_DONEREAD = BAR_PART + 1;   // split K/V: the first part has read this one's partial
+    static constexpr int NBARS = BAR_DONEREAD + 1;
+    // split K/V: a part's partial results, staged in the (then idle) K/V ring:
+    // unnormalised O rows (float32, padded stride) and the per-row m, l_exact, l_round
+    static constexpr int PSTR = D + 4;
+    static constexpr int PART_BYTES = (NQ * 128 * PSTR + 3 * NQ * 128) * 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 
@@ -109,6 +115,7 @@ struct TcShape {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(!SPLIT_REGS || 2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER == THREADS * LAUNCH_REGS,
                   "register split must equal the launch allocation");
+    static constexpr bool CAN_SPLIT = (PART_BYTES <= NS * SLOT_BYTES) && (BR == 128);
 };
 
 struct TcParams {
@@ -120,6 +127,11 @@ struct TcParams {
     const float *key_mask;  // [BH][N] additive, or null
     float *lse;             // [BH][N], or null
     int *err;               // device error word
+    // Work items (groups of NQ query tiles) are numbered in launch order.
+    // Items [0, n_full) run whole; every later item is split along K/V into
+    // `split` parts run by the `split` CTAs of one cluster, merged by part 0.
+    int n_full;
+    int split;
 };
 
 template <int D, int BR, int BC, int NQ, bool MASKED>
@@ -135,11 +147,23 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
     const int lane = threadIdx.x & 31;
 
     // ---- work item ----
+    // Causal: heaviest query groups (largest rows) first.  Non-causal: all
+    // query groups of one head together, so a head's K/V stay hot in L2.
     const int lin = blockIdx.x;
-    const int qg = p.num_qg - 1 - lin / p.BH;
-    const int bh = lin % p.BH;
+    int item = lin, part = 0, nparts = 1;
+    if (lin >= p.n_full) {
+        const int t = lin - p.n_full;
+        item = p.n_full + t / p.split;
+        part = t % p.split;   // equals the rank in the cluster
+        nparts = p.split;
+    }
+    const int qg = p.causal ? p.num_qg - 1 - item / p.BH : item % p.num_qg;
+    const int bh = p.causal ? item % p.BH : item / p.num_qg;
     const int N = p.N;
     const int nkv_all = (N + BC - 1) / BC;
+    // this CTA's K/V tiles: [kv_lo, kv_lo + nkv) (a part's share of a split item)
+    const int kv_lo = static_cast<int>((static_cast<long long>(nkv_all) * part) / nparts);
+    const int kv_hi = static_cast<int>((static_cast<long long>(nkv_all) * (part + 1)) / nparts);
     int r0[NQ], nkv[NQ];
     int nkv_max = 0;
 #pragma unroll
@@ -151,7 +175,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             const int last_row = min(r0[q] + BR - 1, N - 1);
             nkv[q] = min(nkv_all, last_row / BC + 1);
         } else {
-            nkv[q] = nkv_all;
+            nkv[q] = kv_hi - kv_lo;
         }
         nkv_max = max(nkv_max, nkv[q]);
     }
@@ -174,6 +198,8 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             mbar_init(bar(S::BAR_EMPTY + s), 1);
         }
         mbar_init(bar(S::BAR_DONE), 1);
+        mbar_init(bar(S::BAR_PART), static_cast<uint32_t>((nparts > 1 ? nparts - 1 : 1) * NQ * 128));
+        mbar_init(bar(S::BAR_DONEREAD), 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -185,6 +211,11 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if constexpr (S::CAN_SPLIT) {
+        // Parts of a split item arrive on each other's barriers: all of the
+        // cluster's barriers must be initialised first.
+        if (nparts > 1) cluster_sync();
+    }
 
     if (warp >= S::SOFTMAX_WARPS) {
         if constexpr (S::SPLIT_REGS) regs_dec<S::REGS_OTHER>();
@@ -231,7 +262,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
 #pragma unroll
                     for (int cb = 0; cb < S::CB; ++cb)
                         tma_load_3d_hint(sRing + slot * S::SLOT_BYTES + cb * (BC * 128), m,
-                                         bar(S::BAR_FULL + slot), cb * 64, j * BC, bh, pol_kv);
+                                         bar(S::BAR_FULL + slot), cb * 64, (kv_lo + j) * BC, bh, pol_kv);
                 }
                 issued = t + 1;
             }
@@ -355,7 +386,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
         for (int j = 0; j < nkv[q]; ++j) {
             if (!mbar_wait(bar(S::BAR_SFULL + q), j & 1, abort_flag, p.err, 20)) { ok = false; break; }
             tc_fence_after();
-            const int key0 = j * BC;
+            const int key0 = (kv_lo + j) * BC;
             // Tiles that need per-element masking: the N tail, the causal
             // diagonal, or any tile when a key mask is given.
             const bool edge = MASKED || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0[q]);
@@ -575,11 +606,77 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
         }
 
         // ---------------- epilogue ----------------
-        if (nkv[q] > 0) {
-            if (ok) ok = mbar_wait(bar(S::BAR_OFULL + q), 0, abort_flag, p.err, 21);
-            tc_fence_after();
-            const bool any = (l_exact > 0.f) && (l_round > 0.f);
-            const float inv = any ? 1.f / l_round : 0.f;
+        // A split item: every part but the first publishes its partial result
+        // (unnormalised O, m, l_exact, l_round per row) in its own shared
+        // memory; the first part merges them with its own, with the same
+        // rescale as between tiles: M = max_p m_p, weights 2^(m_p - M).
+        if (nkv[q] > 0 && ok) ok = mbar_wait(bar(S::BAR_OFULL + q), 0, abort_flag, p.err, 21);
+        tc_fence_after();
+        float a_own = 1.f;                 // weight of this CTA's O
+        float a_part[8];                   // weights of the other parts' O
+        float le_fin = l_exact, lr_fin = l_round, m_fin = m;
+        bool write_out = true;
+        const uint32_t sPart = sRing;      // partials live in the (now idle) K/V ring
+        const uint32_t part_row = sPart + ((q * 128 + row_in) * S::PSTR) * 4;
+        auto stat_addr = [&](int k) { return sPart + (NQ * 128 * S::PSTR + k * NQ * 128 + q * 128 + row_in) * 4; };
+#pragma unroll
+        for (int pp = 0; pp < 8; ++pp) a_part[pp] = 0.f;
+        if constexpr (S::CAN_SPLIT) {
+            if (nparts > 1 && part > 0) {
+                // The ring is reused only after every MMA of the CTA (both query
+                // tiles) has completed: the other tile's last PV may still read V.
+                mbar_wait(bar(S::BAR_DONE), 0, abort_flag, p.err, 24);
+                tc_fence_after();
+                if (nkv[q] > 0) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + 32 * c, o);
+                        tmem_ld_wait();
+                        reg_fence32(o);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(part_row + (32 * c + 4 * k) * 4),
+                                         "r"(o[4 * k]), "r"(o[4 * k + 1]), "r"(o[4 * k + 2]), "r"(o[4 * k + 3])
+                                         : "memory");
+                    }
+                }
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(0)), "f"(m) : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(1)), "f"(l_exact) : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(2)), "f"(l_round) : "memory");
+                mbar_arrive_remote(mapa_shared(bar(S::BAR_PART), 0));
+                // this CTA's shared memory must outlive the first part's reads
+                mbar_wait_cluster(bar(S::BAR_DONEREAD), 0, abort_flag, p.err, 22);
+                write_out = false;
+            } else if (nparts > 1) {
+                mbar_wait_cluster(bar(S::BAR_PART), 0, abort_flag, p.err, 23);
+                float mp[8], lep[8], lrp[8];
+                m_fin = m;
+                for (int pp = 1; pp < nparts; ++pp) {
+                    mp[pp] = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
+                    lep[pp] = ld_cluster_f32(mapa_shared(stat_addr(1), pp));
+                    lrp[pp] = ld_cluster_f32(mapa_shared(stat_addr(2), pp));
+                    m_fin = fmaxf(m_fin, mp[pp]);
+                }
+                if (m_fin == kNegInf) {
+                    a_own = 0.f;
+                    le_fin = 0.f;
+                    lr_fin = 0.f;
+                } else {
+                    a_own = (m == kNegInf) ? 0.f : ex2(m - m_fin);
+                    le_fin = a_own * l_exact;
+                    lr_fin = a_own * l_round;
+                    for (int pp = 1; pp < nparts; ++pp) {
+                        a_part[pp] = (mp[pp] == kNegInf) ? 0.f : ex2(mp[pp] - m_fin);
+                        le_fin += a_part[pp] * lep[pp];
+                        lr_fin += a_part[pp] * lrp[pp];
+                    }
+                }
+            }
+        }
+        if (nkv[q] > 0 && write_out) {
+            const bool any = (le_fin > 0.f) && (lr_fin > 0.f);
+            const float inv = any ? 1.f / lr_fin : 0.f;
             const uint64_t inv2 = f2_pack(inv, inv);
             const uint32_t stage = sQ + q * S::Q_BYTES;  // Q_q is no longer read
 #pragma unroll
@@ -588,6 +685,27 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                 tmem_ld32(tO + 32 * c, o);
                 tmem_ld_wait();
                 reg_fence32(o);
+                if constexpr (S::CAN_SPLIT) {
+                    if (nparts > 1) {
+                        // O = a_own O_own + sum_p a_p O_p (other parts read from
+                        // their shared memory through the cluster)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a_own);
+                        for (int pp = 1; pp < nparts; ++pp) {
+                            if (a_part[pp] == 0.f) continue;
+                            const uint32_t src = mapa_shared(part_row + 32 * c * 4, pp);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                float v0, v1, v2, v3;
+                                ld_cluster_v4(src + 16 * k, v0, v1, v2, v3);
+                                o[4 * k] = __float_as_uint(fmaf(a_part[pp], v0, __uint_as_float(o[4 * k])));
+                                o[4 * k + 1] = __float_as_uint(fmaf(a_part[pp], v1, __uint_as_float(o[4 * k + 1])));
+                                o[4 * k + 2] = __float_as_uint(fmaf(a_part[pp], v2, __uint_as_float(o[4 * k + 2])));
+                                o[4 * k + 3] = __float_as_uint(fmaf(a_part[pp], v3, __uint_as_float(o[4 * k + 3])));
+                            }
+                        }
+                    }
+                }
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -619,7 +737,16 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                 tma_store_wait_read0();
             }
             if (active && p.lse != nullptr && row < N) {
-                p.lse[static_cast<size_t>(bh) * N + row] = any ? (m + log2f(l_exact)) * kLn2 : kNegInf;
+                p.lse[static_cast<size_t>(bh) * N + row] = any ? (m_fin + log2f(le_fin)) * kLn2 : kNegInf;
+            }
+        }
+        if constexpr (S::CAN_SPLIT) {
+            if (nparts > 1 && part == 0) {
+                // every softmax thread of the first part has read the other
+                // parts' shared memory: they may exit
+                named_bar_sync(5, NQ * 128);
+                if (threadIdx.x == 0)
+                    for (int pp = 1; pp < nparts; ++pp) mbar_arrive_remote(mapa_shared(bar(S::BAR_DONEREAD), pp));
             }
         }
     }
@@ -645,9 +772,20 @@ bool make_map(CUtensorMap *m, const void *base, int D, int N, int BH, int box_ro
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count(int dev) {
+    static int counts[64];
+    if (dev < 0 || dev >= 64) return 0;
+    if (counts[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
 template <int D, int BR, int BC, int NQ, bool MASKED>
 int launch_variant(const void *Q, const void *K, const void *V, void *O, float *LSE, int BH, int N,
-                   int causal, float scale, const float *key_mask, cudaStream_t stream) {
+                   int causal, float scale, const float *key_mask, cudaStream_t stream, int *split_out) {
     using S = TcShape<D, BR, BC, NQ, MASKED>;
     auto kern = attn_fwd_tc_kernel<D, BR, BC, NQ, MASKED>;
     static int attr_device = -1;
@@ -679,9 +817,51 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
     p.lse = LSE;
     p.err = device_error_word();
     if (!p.err) return kErrCuda;
-    const long long grid = static_cast<long long>(p.num_qg) * BH;
+    // One CTA per SM: the items beyond the last full wave are split along K/V
+    // into s parts (a cluster of s CTAs each) so that the tail wave is as
+    // short as the SMs allow.  Causal work is uneven and stays unsplit.
+    const long long items = static_cast<long long>(p.num_qg) * BH;
+    if (items > 0x7fffffffLL) return kErrUnsupported;
+    int split = 1;
+    long long n_full = items;
+    const int nsm = sm_count(dev);
+    if (S::CAN_SPLIT && !causal && nsm > 0) {
+        const long long R = items % nsm;
+        const int nkv_all = (N + BC - 1) / BC;
+        int sp = 1;
+        while (R > 0 && sp * 2 <= 8 && sp * 2 * R <= nsm && sp * 2 <= nkv_all) sp *= 2;
+        if (sp > 1 && (items - R) % sp == 0) {
+            split = sp;
+            n_full = items - R;
+        }
+    }
+    p.n_full = static_cast<int>(n_full);
+    p.split = split;
+    const long long grid = n_full + (items - n_full) * split;
     if (grid > 0x7fffffffLL) return kErrUnsupported;
-    kern<<<static_cast<unsigned>(grid), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
+    if (split > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(S::THREADS);
+        cfg.dynamicSmemBytes = S::SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, p) == cudaSuccess) {
+            if (split_out) *split_out = split;
+            return kOk;
+        }
+        (void)cudaGetLastError();   // cluster not schedulable: run unsplit
+        p.n_full = static_cast<int>(items);
+        p.split = 1;
+    }
+    if (split_out) *split_out = 1;
+    kern<<<static_cast<unsigned>(items), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
@@ -689,13 +869,17 @@ template <int D, int BR, int BC>
 int launch_shape(const void *Q, const void *K, const void *V, void *O, float *LSE, int BH, int N, int causal,
                  float scale, const float *key_mask, cudaStream_t stream, const char **variant) {
     constexpr int NQ = (2 * (BC + D) <= 512) ? 2 : 1;
-    static char names[2][64];
-    char *name = names[key_mask ? 1 : 0];
-    snprintf(name, 64, "tc_bf16_d%d_br%d_bc%d_nq%d%s", D, BR, BC, NQ, key_mask ? "_mask" : "");
+    static char names[2][4][64];
+    int split = 1;
+    const int rc = key_mask
+        ? launch_variant<D, BR, BC, NQ, true>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, &split)
+        : launch_variant<D, BR, BC, NQ, false>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream, &split);
+    const int si = split >= 8 ? 3 : split >= 4 ? 2 : split >= 2 ? 1 : 0;
+    char *name = names[key_mask ? 1 : 0][si];
+    snprintf(name, 64, "tc_bf16_d%d_br%d_bc%d_nq%d%s%s", D, BR, BC, NQ, key_mask ? "_mask" : "",
+             si == 0 ? "" : si == 1 ? "_kvsplit2" : si == 2 ? "_kvsplit4" : "_kvsplit8");
     if (variant) *variant = name;
-    if (key_mask)
-        return launch_variant<D, BR, BC, NQ, true>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream);
-    return launch_variant<D, BR, BC, NQ, false>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask, stream);
+    return rc;
 }
 
 template <int D, int BR>

@@ -70,6 +70,20 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
     return ok != 0;
 }
 
+// try_wait with acquire at cluster scope: after it succeeds, writes that other
+// CTAs of the cluster released with their (remote) arrives are visible.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns`, or as soon as *abort is non-zero (another thread of the CTA
 // already gave up); then records the site in the error word, raises *abort
@@ -99,6 +113,58 @@ __device__ __forceinline__ bool elect_one() {
         "selp.u32 %0, 1, 0, P;\n\t}"
         : "=r"(pred));
     return pred != 0;
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters: distributed shared memory and remote arrives
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of all CTAs of the cluster (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void ld_cluster_v4(uint32_t caddr, float &a, float &b, float &c, float &d) {
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(a), "=f"(b), "=f"(c), "=f"(d)
+                 : "r"(caddr)
+                 : "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+    return v;
+}
+// Arrive on an mbarrier in another CTA of the cluster; orders this thread's
+// earlier shared-memory writes before the arrive at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+// Bounded wait with cluster-scope acquire (see mbar_wait).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile uint32_t *abort,
+                                                  int *err, int site, unsigned long long limit_ns = kWaitLimitNs) {
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 63u) == 63u) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
+                atomicOr(err, kErrTimeout | (site << 8));
+                *abort = 1u;
+                return false;
+            }
+        }
+    }
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32).
