@@ -39,6 +39,25 @@ WORKLOAD = "bf16_2x16x4096x128"
 N_SETS = 4
 
 
+def ncu_traffic():
+    """DRAM bytes per launch of the bench kernel from the committed ncu record,
+    or None if the kernel sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "attn_fwd_tc_bf16_2x16x4096x128_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for src in rec["source_files"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["source_sha256"]:
+            return None
+        return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+    except Exception:
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -301,7 +320,9 @@ def main():
                          "(each step reads data not in L2)"},
         "pct_of_peak": 100.0 * value / world / pk["bf16_tflops"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                     "frac": achieved / pk["bf16_tflops"], "traffic": ncu_traffic(),
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
+                     "algorithmic_bytes": 4 * w.B * w.H * w.N * w.d * 2 + 4 * w.B * w.H * w.N,
                      "peak_source": f"{pk['source']} bf16 burst", "kernel_ms": avg_kernel_ms},
         "hbm_gbs": (4 * w.B * w.H * w.N * w.d * 2 + 4 * w.B * w.H * w.N) / (avg_kernel_ms / 1e3) / 1e9,
         "gpu_launches": args.steps,
