@@ -22,9 +22,13 @@
 //                  needed, writes P_q as bf16 back over S_q's columns, then
 //                  the epilogue (normalise, bf16, TMA store; LSE).
 // The MMA issue order S_0(j+1) after PV_0(j), S_1(j+1) after PV_1(j) lets the
-// tensor pipe work on one tile while the other tile's softmax runs.  With two
-// query tiles the softmax warpgroups take 208 registers per thread with
-// setmaxnreg and the producer/MMA warpgroup gives its share back.
+// tensor pipe work on one tile while the other tile's softmax runs.  With
+// BC = 128 the softmax hands P over in two halves, so the first half's P V runs
+// while the second half is exponentiated.  With BC = 64 each query tile has
+// two S buffers in tensor memory and S_q(j+2) is issued right after P_q V_j, so
+// the softmax of one tile never waits for its own P V.  Where the 128-column
+// softmax needs more than the launch share of registers, setmaxnreg moves
+// registers from the producer/MMA warpgroup to the softmax warpgroups.
 //
 // BR = 64 uses M = 64 MMAs, whose accumulator rows r sit in tensor-memory lane
 // 32*(r/16) + r%16: lanes 0..15 of each warp carry rows, lanes 16..31 idle.
@@ -65,7 +69,15 @@ struct TcShape {
     static constexpr int MASK_BYTES = MASKED ? NQ * 2 * BC * 4 : 0;
     static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES - MASK_BYTES) / SLOT_BYTES;
     static constexpr int NS = NS_RAW > 8 ? 8 : (NS_RAW < 2 ? 2 : NS_RAW);
-    static constexpr int TMEM_USED = NQ * (BC + D);
+    // Two S buffers per query tile when tensor memory has room (BC = 64 with
+    // two query tiles): S_q(j+2) is computed while the softmax works on S_q(j+1)
+    // and P_q(j) waits for its P V, instead of after P V.
+    static constexpr bool DBS = (NQ == 2) && (2 * NQ * BC + NQ * D <= 512);
+    static constexpr int NSB = DBS ? 2 : 1;
+    // With one S buffer and BC = 128, P is handed to the MMA in two halves: the
+    // first half's P V runs while the softmax works on the second half.
+    static constexpr int NP = (!DBS && BC == 128) ? 2 : 1;
+    static constexpr int TMEM_USED = NQ * (NSB * BC + D);
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32
                                      : TMEM_USED <= 64 ? 64
                                      : TMEM_USED <= 128 ? 128
@@ -76,6 +88,12 @@ struct TcShape {
     // Two query tiles: a third full warpgroup (TMA, MMA, 2 idle) so that
     // setmaxnreg can move registers between whole warpgroups.
     static constexpr bool SPLIT_REGS = (NQ == 2);
+    // setmaxnreg moves registers from the producer/MMA warpgroup to the softmax
+    // warpgroups where the 128-column softmax does not fit the launch share
+    // (168) without spilling; where it does fit (and for BC = 64) the move
+    // would only make the MMA issuer spill.  Chosen per shape from ptxas's
+    // spill counts.
+    static constexpr bool MOVE_REGS = SPLIT_REGS && BC == 128 && !(D == 128 && BR == 128 && !MASKED);
     static constexpr int THREADS = SPLIT_REGS ? 384 : 32 * (SOFTMAX_WARPS + 2);
     static constexpr int LAUNCH_REGS = 168;          // 65536 / 384, rounded down to 8
     static constexpr int REGS_SOFTMAX = 208;
@@ -85,26 +103,32 @@ struct TcShape {
     static constexpr int OFF_RING = NQ * Q_BYTES;
     static constexpr int OFF_MASK = OFF_RING + NS * SLOT_BYTES;
     static constexpr int OFF_BAR = OFF_MASK + MASK_BYTES;
-    // barriers: q_full[NQ] full[NS] empty[NS] s_full[NQ] p_full[NQ] o_full[NQ] done part done_read
+    // barriers: q_full[NQ] full[NS] empty[NS] s_full[NQ][NSB] p_full[NQ][NSB][NP] o_full[NQ]
+    // pv_done[NQ] done part done_read
     static constexpr int BAR_QFULL = 0;
     static constexpr int BAR_FULL = BAR_QFULL + NQ;
     static constexpr int BAR_EMPTY = BAR_FULL + NS;
     static constexpr int BAR_SFULL = BAR_EMPTY + NS;
-    static constexpr int BAR_PFULL = BAR_SFULL + NQ;
-    static constexpr int BAR_OFULL = BAR_PFULL + NQ;
-    static constexpr int BAR_DONE = BAR_OFULL + NQ;
+    static constexpr int BAR_PFULL = BAR_SFULL + NQ * NSB;
+    static constexpr int BAR_OFULL = BAR_PFULL + NQ * NSB * NP;
+    // two S buffers: each P_q V has completed; P in two halves: the first half's P_q V has completed
+    static constexpr int BAR_PVDONE = BAR_OFULL + NQ;
+    static constexpr int BAR_DONE = BAR_PVDONE + NQ;
     static constexpr int BAR_PART = BAR_DONE + 1;       // split K/V: partials of the other parts are ready
     static constexpr int BAR_DONEREAD = BAR_PART + 1;   // split K/V: the first part has read this one's partial
     static constexpr int NBARS = BAR_DONEREAD + 1;
-    // split K/V: a part's partial results, staged in the (then idle) K/V ring:
+    // split K/V: a part's partial results, staged in the (then idle) Q tiles and K/V ring:
     // unnormalised O rows (float32, padded stride) and the per-row m, l_exact, l_round
     static constexpr int PSTR = D + 4;
     static constexpr int PART_BYTES = (NQ * 128 * PSTR + 3 * NQ * 128) * 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+    // + alignment slack; a 512-column tensor-memory user also claims enough
+    // shared memory that no second CTA can be resident (its allocation would wait)
+    static constexpr int SMEM_MIN = OFF_MISC + 16 + 1024;
+    static constexpr int SMEM_BYTES = (TMEM_COLS == 512 && SMEM_MIN <= 116 * 1024) ? 117 * 1024 : SMEM_MIN;
 
-    __host__ __device__ static constexpr int s_col(int q) { return q * BC; }
-    __host__ __device__ static constexpr int o_col(int q) { return NQ * BC + q * D; }
+    __host__ __device__ static constexpr int s_col(int q, int b) { return (q * NSB + b) * BC; }
+    __host__ __device__ static constexpr int o_col(int q) { return NQ * NSB * BC + q * D; }
 
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(BR == 64 || BR == 128, "query tile");
@@ -113,9 +137,11 @@ struct TcShape {
     // A 512-column allocation must never wait for another resident CTA.
     static_assert(TMEM_COLS < 512 || SMEM_BYTES > 116 * 1024, "one CTA per SM for full TMEM");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-    static_assert(!SPLIT_REGS || 2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER == THREADS * LAUNCH_REGS,
+    static_assert(!MOVE_REGS || 2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER == THREADS * LAUNCH_REGS,
                   "register split must equal the launch allocation");
-    static constexpr bool CAN_SPLIT = (PART_BYTES <= NS * SLOT_BYTES) && (BR == 128);
+    // two S buffers: K_{j+2} is waited for while V_j still holds its slot
+    static_assert(!DBS || NS >= 4, "ring depth for two S buffers");
+    static constexpr bool CAN_SPLIT = (PART_BYTES <= NQ * Q_BYTES + NS * SLOT_BYTES) && (BR == 128);
 };
 
 struct TcParams {
@@ -189,9 +215,12 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int q = 0; q < NQ; ++q) {
             mbar_init(bar(S::BAR_QFULL + q), 1);
-            mbar_init(bar(S::BAR_SFULL + q), 1);
-            mbar_init(bar(S::BAR_PFULL + q), 128);
+            for (int b = 0; b < S::NSB; ++b) {
+                mbar_init(bar(S::BAR_SFULL + q * S::NSB + b), 1);
+                for (int h = 0; h < S::NP; ++h) mbar_init(bar(S::BAR_PFULL + (q * S::NSB + b) * S::NP + h), 128);
+            }
             mbar_init(bar(S::BAR_OFULL + q), 1);
+            mbar_init(bar(S::BAR_PVDONE + q), 1);
         }
         for (int s = 0; s < S::NS; ++s) {
             mbar_init(bar(S::BAR_FULL + s), 1);
@@ -218,7 +247,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
     }
 
     if (warp >= S::SOFTMAX_WARPS) {
-        if constexpr (S::SPLIT_REGS) regs_dec<S::REGS_OTHER>();
+        if constexpr (S::MOVE_REGS) regs_dec<S::REGS_OTHER>();
         // The producer and MMA warps run their loops on all 32 lanes with
         // warp-uniform values (so address and descriptor arithmetic stays on
         // the uniform datapath) and one elected lane issues each copy, MMA
@@ -288,26 +317,30 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
             const uint64_t kdesc0 = sdesc_sw128(sRing, 16, 1024);
             const uint64_t vdesc0 = sdesc_sw128(sRing, BC * 128, 1024);
+            // S_q(j) goes to S buffer j % NSB and is signalled on that buffer's barrier.
             auto issue_s = [&](int q, int j) {
+                const int b = j & (S::NSB - 1);
                 const uint64_t a0 = qdesc0 + static_cast<uint64_t>((q * S::Q_BYTES) >> 4);
                 const uint64_t b0 = kdesc0 + static_cast<uint64_t>((((2 * j) % S::NS) * S::SLOT_BYTES) >> 4);
                 if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int cb = kk >> 2, off = (kk & 3) * 32;
-                        mma_bf16_ss(tmem + S::s_col(q), a0 + static_cast<uint64_t>((cb * (BR * 128) + off) >> 4),
+                        mma_bf16_ss(tmem + S::s_col(q, b), a0 + static_cast<uint64_t>((cb * (BR * 128) + off) >> 4),
                                     b0 + static_cast<uint64_t>((cb * (BC * 128) + off) >> 4), idesc_s,
                                     kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(bar(S::BAR_SFULL + q));
+                    tc_commit(bar(S::BAR_SFULL + q * S::NSB + b));
                 }
             };
-            auto issue_pv = [&](int q, int j) {
+            // P_q V_j over K steps [BC/16 * h / NP, BC/16 * (h+1) / NP): part h of P
+            auto issue_pv = [&](int q, int j, int h) {
+                const int b = j & (S::NSB - 1);
                 const uint64_t b0 = vdesc0 + static_cast<uint64_t>((((2 * j + 1) % S::NS) * S::SLOT_BYTES) >> 4);
                 if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < BC / 16; ++kk) {
-                        mma_bf16_ts(tmem + S::o_col(q), tmem + S::s_col(q) + kk * 8,
+                    for (int kk = (BC / 16) * h / S::NP; kk < (BC / 16) * (h + 1) / S::NP; ++kk) {
+                        mma_bf16_ts(tmem + S::o_col(q), tmem + S::s_col(q, b) + kk * 8,
                                     b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_o,
                                     (j > 0 || kk > 0) ? 1u : 0u);
                     }
@@ -317,44 +350,97 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                 if (leader) tc_commit(bar(b));
             };
 
-            if (ok && nkv_max > 0) {
-                ok = wwait(bar(S::BAR_FULL + 0), 0, 11);  // K_0
-                if (ok) {
-                    tc_fence_after();
-                    for (int q = 0; q < NQ; ++q)
-                        if (nkv[q] > 0) issue_s(q, 0);
-                    commit(S::BAR_EMPTY + 0);
-                }
-            }
-            for (int j = 0; ok && j < nkv_max; ++j) {
-                const int tv = 2 * j + 1;
-                if (!wwait(bar(S::BAR_FULL + tv % S::NS), (tv / S::NS) & 1, 12)) break;
-                tc_fence_after();
-                bool k_ready = false;
-                const int tk = 2 * j + 2;
-                for (int q = 0; q < NQ && ok; ++q) {
-                    if (j >= nkv[q]) continue;
-                    if (!wwait(bar(S::BAR_PFULL + q), j & 1, 13)) {
+            if constexpr (S::DBS) {
+                // Two S buffers per query tile.  Order: S(0), S(1) for both
+                // tiles; then per step j: P_0 V_j, S_0(j+2), P_1 V_j, S_1(j+2).
+                // S_q(j+2) overwrites the buffer P_q(j) was read from, after it
+                // in the tensor pipe; it is ready long before the softmax wants
+                // it, so the softmax never waits for P V.
+                for (int jj = 0; ok && jj < 2 && jj < nkv_max; ++jj) {
+                    const int tk = 2 * jj;
+                    if (!wwait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, 11)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_pv(q, j);
-                    if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
-                    if (j + 1 < nkv[q]) {
-                        if (!k_ready) {
-                            if (!wwait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, 14)) {
+                    for (int q = 0; q < NQ; ++q)
+                        if (jj < nkv[q]) issue_s(q, jj);
+                    commit(S::BAR_EMPTY + tk % S::NS);
+                }
+                for (int j = 0; ok && j < nkv_max; ++j) {
+                    const int tv = 2 * j + 1, tk = 2 * j + 4;
+                    if (!wwait(bar(S::BAR_FULL + tv % S::NS), (tv / S::NS) & 1, 12)) break;
+                    tc_fence_after();
+                    bool k_ready = false;
+                    for (int q = 0; q < NQ && ok; ++q) {
+                        if (j >= nkv[q]) continue;
+                        if (!wwait(bar(S::BAR_PFULL + q * S::NSB + (j & 1)), (j >> 1) & 1, 13)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(q, j, 0);
+                        commit(S::BAR_PVDONE + q);
+                        if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
+                        if (j + 2 < nkv[q]) {
+                            if (!k_ready) {
+                                if (!wwait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, 14)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                k_ready = true;
+                            }
+                            issue_s(q, j + 2);
+                        }
+                    }
+                    commit(S::BAR_EMPTY + tv % S::NS);               // V_j slot
+                    if (k_ready) commit(S::BAR_EMPTY + tk % S::NS);  // K_{j+2} slot
+                }
+            } else {
+                if (ok && nkv_max > 0) {
+                    ok = wwait(bar(S::BAR_FULL + 0), 0, 11);  // K_0
+                    if (ok) {
+                        tc_fence_after();
+                        for (int q = 0; q < NQ; ++q)
+                            if (nkv[q] > 0) issue_s(q, 0);
+                        commit(S::BAR_EMPTY + 0);
+                    }
+                }
+                for (int j = 0; ok && j < nkv_max; ++j) {
+                    const int tv = 2 * j + 1;
+                    if (!wwait(bar(S::BAR_FULL + tv % S::NS), (tv / S::NS) & 1, 12)) break;
+                    tc_fence_after();
+                    bool k_ready = false;
+                    const int tk = 2 * j + 2;
+                    for (int q = 0; q < NQ && ok; ++q) {
+                        if (j >= nkv[q]) continue;
+                        for (int h = 0; h < S::NP && ok; ++h) {
+                            if (!wwait(bar(S::BAR_PFULL + q * S::NP + h), j & 1, 13)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            k_ready = true;
+                            issue_pv(q, j, h);
+                            if (S::NP > 1 && h == 0) commit(S::BAR_PVDONE + q);
                         }
-                        issue_s(q, j + 1);
+                        if (!ok) break;
+                        if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
+                        if (j + 1 < nkv[q]) {
+                            if (!k_ready) {
+                                if (!wwait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, 14)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                k_ready = true;
+                            }
+                            issue_s(q, j + 1);
+                        }
                     }
+                    commit(S::BAR_EMPTY + tv % S::NS);               // V_j slot
+                    if (k_ready) commit(S::BAR_EMPTY + tk % S::NS);  // K_{j+1} slot
                 }
-                commit(S::BAR_EMPTY + tv % S::NS);               // V_j slot
-                if (k_ready) commit(S::BAR_EMPTY + tk % S::NS);  // K_{j+1} slot
             }
             // Every MMA issued has completed before tensor memory is released.
             commit(S::BAR_DONE);
@@ -365,16 +451,24 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
         // ------------------------------------------------------------------
         // Softmax warpgroup of query tile q
         // ------------------------------------------------------------------
-        if constexpr (S::SPLIT_REGS) regs_inc<S::REGS_SOFTMAX>();
+        if constexpr (S::MOVE_REGS) regs_inc<S::REGS_SOFTMAX>();
         const int q = warp >> 2;
         const int wq = warp & 3;
+        // This tile's row offset and K/V tile count as plain registers (a
+        // run-time index into r0[] / nkv[] would place them in local memory).
+        int r0q = r0[0], nkvq = nkv[0];
+#pragma unroll
+        for (int i = 1; i < NQ; ++i)
+            if (q == i) {
+                r0q = r0[i];
+                nkvq = nkv[i];
+            }
         // Row of this thread.  M = 128: lane l of warp w holds row 32w + l.
         // M = 64: lanes 0..15 of warp w hold rows 16w .. 16w+15.
         const bool active = (BR == 128) || (lane < 16);
         const int row_in = (BR == 128) ? wq * 32 + lane : wq * 16 + (lane & 15);
-        const int row = r0[q] + row_in;
+        const int row = r0q + row_in;
         const uint32_t t_lane = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t tS = tmem + t_lane + S::s_col(q);
         const uint32_t tO = tmem + t_lane + S::o_col(q);
         const float sl2 = p.scale_log2;
         const float *mrow = MASKED ? p.key_mask + static_cast<size_t>(bh) * N : nullptr;
@@ -383,15 +477,20 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
         float l_round = 0.f;  // sum of the bf16-rounded p used in P V (normalises O)
         bool ok = true;
 
-        for (int j = 0; j < nkv[q]; ++j) {
-            if (!mbar_wait(bar(S::BAR_SFULL + q), j & 1, abort_flag, p.err, 20)) { ok = false; break; }
+        for (int j = 0; j < nkvq; ++j) {
+            const int sb = j & (S::NSB - 1);   // S buffer of this tile
+            if (!mbar_wait(bar(S::BAR_SFULL + q * S::NSB + sb), (j / S::NSB) & 1, abort_flag, p.err, 20)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
+            const uint32_t tS = tmem + t_lane + S::s_col(q, sb);
             const int key0 = (kv_lo + j) * BC;
             // Tiles that need per-element masking: the N tail, the causal
             // diagonal, or any tile when a key mask is given.
-            const bool edge = MASKED || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0[q]);
+            const bool edge = MASKED || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0q);
 
-            const bool diag = p.causal && key0 + BC - 1 > r0[q];   // tile crosses the causal diagonal
+            const bool diag = p.causal && key0 + BC - 1 > r0q;   // tile crosses the causal diagonal
             // Key mask of this tile, once per warpgroup, in log2 units with -inf
             // past N; double-buffered so one barrier per tile suffices.
             const float *msm = reinterpret_cast<const float *>(smem + S::OFF_MASK) + (q * 2 + (j & 1)) * BC;
@@ -472,99 +571,166 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             };
 
             constexpr bool kTwoPass = BC > 128;   // 256 columns do not fit in registers
-            float tile_ls = 0.f, tile_lr = 0.f;
-            float alpha = 1.f;
+            // Before O_q is rescaled it must hold every P V issued so far: the
+            // one of tile j-1 may still run with two S buffers, and the first
+            // half of this tile's P may be in flight once handed over.
+            auto o_settled = [&](int part) {
+                if constexpr (S::DBS) {
+                    mbar_wait(bar(S::BAR_PVDONE + q), (j - 1) & 1, abort_flag, p.err, 25);
+                    tc_fence_after();
+                } else if constexpr (S::NP > 1) {
+                    if (part > 0) {
+                        mbar_wait(bar(S::BAR_PVDONE + q), j & 1, abort_flag, p.err, 25);
+                        tc_fence_after();
+                    }
+                }
+            };
+            // Part `part` of P_q is in tensor memory: its P V may be issued.
+            auto release_p = [&](int part) {
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(S::BAR_PFULL + (q * S::NSB + sb) * S::NP + part));
+            };
             if constexpr (!kTwoPass) {
-                uint32_t sr[BC];
+                // S is read from tensor memory in groups of HC columns; the load
+                // of the next group is in flight while one is exponentiated.
+                constexpr int HC = BC < 64 ? BC : 64;
+                constexpr int NG = BC / HC;
+                constexpr int GPP = NG / S::NP;     // groups per part of P
+                static_assert(NG % S::NP == 0, "parts of P");
                 uint32_t pk[BC / 2];
-                auto load_tile = [&]() {
+                auto issue_group = [&](int g, uint32_t *sr) {
 #pragma unroll
-                    for (int c = 0; c < BC / 32; ++c) tmem_ld32(tS + 32 * c, sr + 32 * c);
-                    tmem_ld_wait();
+                    for (int c = 0; c < HC / 32; ++c) tmem_ld32(tS + HC * g + 32 * c, sr + 32 * c);
+                };
+                // after the wait: scale/masks where needed
+                auto finish_group = [&](int g, uint32_t *sr) {
 #pragma unroll
-                    for (int c = 0; c < BC / 32; ++c) reg_fence32(sr + 32 * c);
+                    for (int c = 0; c < HC / 32; ++c) reg_fence32(sr + 32 * c);
                     if (edge) {
 #pragma unroll
-                        for (int c = 0; c < BC / 32; ++c) mask_chunk(c, sr + 32 * c);
+                        for (int c = 0; c < HC / 32; ++c) mask_chunk((HC / 32) * g + c, sr + 32 * c);
                     }
                 };
-                // p = 2^(x - m_use) for the whole tile into pk (bf16 pairs) and
-                // the two tile sums.
-                auto exps = [&](float m_use) {
+                auto load_group = [&](int g, uint32_t *sr) {
+                    issue_group(g, sr);
+                    tmem_ld_wait();
+                    finish_group(g, sr);
+                };
+                // p = 2^(x - m_use) for the columns of one part of P into pk
+                // (bf16 pairs) and the part's two sums.
+                auto exps = [&](int part, float m_use, float &ls, float &lr) {
                     const uint64_t negm2 = f2_pack(-m_use, -m_use);
                     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-                    tile_ls = 0.f;
-                    tile_lr = 0.f;
+                    ls = 0.f;
+                    lr = 0.f;
+                    uint32_t sbuf[2][HC];
+                    load_group(part * GPP, sbuf[0]);
 #pragma unroll
-                    for (int c = 0; c < BC / 32; ++c) {
-                        uint64_t ls2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
+                    for (int gi = 0; gi < GPP; ++gi) {
+                        const int g = part * GPP + gi;
+                        uint32_t *sr = sbuf[gi & 1];
+                        if (gi + 1 < GPP) issue_group(g + 1, sbuf[(gi + 1) & 1]);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float x0 = __uint_as_float(sr[32 * c + 2 * e]);
-                            const float x1 = __uint_as_float(sr[32 * c + 2 * e + 1]);
-                            const uint64_t xx = f2_pack(x0, x1);
-                            const uint64_t y = edge ? f2_add(xx, negm2) : f2_fma(xx, sl2x2, negm2);
-                            float y0, y1;
-                            f2_unpack(y, y0, y1);
-                            const float p0 = ex2(y0), p1 = ex2(y1);
-                            uint32_t w = pack_bf16x2(p0, p1);
-                            if (!active) w = 0u;
-                            pk[16 * c + e] = w;
-                            ls2 = f2_add(ls2, f2_pack(p0, p1));
-                            lr2 = f2_add(lr2, f2_pack(bf16lo_to_f32(w), bf16hi_to_f32(w)));
+                        for (int c = 0; c < HC / 32; ++c) {
+                            uint64_t ls2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float x0 = __uint_as_float(sr[32 * c + 2 * e]);
+                                const float x1 = __uint_as_float(sr[32 * c + 2 * e + 1]);
+                                const uint64_t xx = f2_pack(x0, x1);
+                                const uint64_t y = edge ? f2_add(xx, negm2) : f2_fma(xx, sl2x2, negm2);
+                                float y0, y1;
+                                f2_unpack(y, y0, y1);
+                                const float p0 = ex2(y0), p1 = ex2(y1);
+                                uint32_t w = pack_bf16x2(p0, p1);
+                                if (!active) w = 0u;
+                                pk[(HC / 2) * g + 16 * c + e] = w;
+                                ls2 = f2_add(ls2, f2_pack(p0, p1));
+                                lr2 = f2_add(lr2, f2_pack(bf16lo_to_f32(w), bf16hi_to_f32(w)));
+                            }
+                            float s0, s1, t0, t1;
+                            f2_unpack(ls2, s0, s1);
+                            f2_unpack(lr2, t0, t1);
+                            ls += s0 + s1;
+                            lr += t0 + t1;
                         }
-                        float s0, s1, t0, t1;
-                        f2_unpack(ls2, s0, s1);
-                        f2_unpack(lr2, t0, t1);
-                        tile_ls += s0 + s1;
-                        tile_lr += t0 + t1;
+                        if (gi + 1 < GPP) {
+                            tmem_ld_wait();
+                            finish_group(g + 1, sbuf[(gi + 1) & 1]);
+                        }
                     }
                 };
-                auto store_p = [&]() {
+                // P chunk c (32 keys) -> S columns 16c .. 16c+15
+                auto store_p = [&](int part) {
 #pragma unroll
-                    for (int c = 0; c < BC / 32; ++c) tmem_st16(tS + 16 * c, pk + 16 * c);
+                    for (int c = part * (BC / 32 / S::NP); c < (part + 1) * (BC / 32 / S::NP); ++c)
+                        tmem_st16(tS + 16 * c, pk + 16 * c);
                 };
-                auto tile_max = [&]() {
+                // maximum over the columns of parts [p0, p1)
+                auto parts_max = [&](int p0, int p1) {
                     float mx = kNegInf;
 #pragma unroll
-                    for (int c = 0; c < BC / 32; ++c) mx = chunk_max(sr + 32 * c, mx);
+                    for (int g = p0 * GPP; g < p1 * GPP; ++g) {
+                        uint32_t sr[HC];
+                        load_group(g, sr);
+#pragma unroll
+                        for (int c = 0; c < HC / 32; ++c) mx = chunk_max(sr + 32 * c, mx);
+                    }
                     return edge ? mx : mx * sl2;   // scale > 0: max commutes with the scaling
                 };
-                load_tile();
                 if (__all_sync(0xffffffffu, !active || m != kNegInf)) {
                     // Every row has a finite reference: exponentiate against it
-                    // in one pass, with no maximum.  A row whose tile sum
-                    // exceeds kFastSumLimit (or overflows) has a score far past
-                    // the reference: only then is the tile's maximum taken and
-                    // the tile redone (S is still intact in tensor memory; P is
-                    // written below).
-                    exps(m);
-                    const bool need = active && !(tile_ls <= kFastSumLimit);
-                    if (!__any_sync(0xffffffffu, need)) {
-                        store_p();
-                    } else {
-                        load_tile();
-                        const float mx = tile_max();
-                        const float m_new = need ? fmaxf(mx, m) : m;
-                        alpha = need ? ex2(m - m_new) : 1.f;
-                        rescale_o(alpha);   // j > 0 here: a finite reference needs an earlier tile
-                        m = m_new;
-                        exps(m);
-                        store_p();
+                    // with no maximum.  A row whose part sum exceeds
+                    // kFastSumLimit (or overflows) has a score far past the
+                    // reference: only then is the part's maximum taken and the
+                    // part redone (its S columns are still intact; its P is
+                    // written after).  Each part of P is released as it is done.
+#pragma unroll
+                    for (int part = 0; part < S::NP; ++part) {
+                        float ls, lr, a = 1.f;
+                        exps(part, m, ls, lr);
+                        const bool need = active && !(ls <= kFastSumLimit);
+                        if (__any_sync(0xffffffffu, need)) {
+                            const float mx = parts_max(part, part + 1);
+                            const float m_new = need ? fmaxf(mx, m) : m;
+                            a = need ? ex2(m - m_new) : 1.f;
+                            o_settled(part);
+                            rescale_o(a);   // j > 0 here: a finite reference needs an earlier tile
+                            m = m_new;
+                            exps(part, m, ls, lr);
+                        }
+                        l_exact = l_exact * a + ls;
+                        l_round = l_round * a + lr;
+                        store_p(part);
+                        release_p(part);
                     }
                 } else {
                     // Maximum first: a row's first tile, or rows with no allowed
-                    // key so far.
-                    const float mx = tile_max();
+                    // key so far.  p <= 2^kRescaleThresh afterwards: no redo.
+                    const float mx = parts_max(0, S::NP);
                     const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
                     const bool moved = (m_new != m);
-                    alpha = moved ? ex2(m - m_new) : 1.f;
-                    if (j > 0 && __any_sync(0xffffffffu, moved)) rescale_o(alpha);
+                    const float a = moved ? ex2(m - m_new) : 1.f;
+                    if (j > 0 && __any_sync(0xffffffffu, moved)) {
+                        o_settled(0);
+                        rescale_o(a);
+                    }
                     m = m_new;
-                    exps(m == kNegInf ? 0.f : m);
-                    store_p();
+                    l_exact *= a;
+                    l_round *= a;
+#pragma unroll
+                    for (int part = 0; part < S::NP; ++part) {
+                        float ls, lr;
+                        exps(part, m == kNegInf ? 0.f : m, ls, lr);
+                        l_exact += ls;
+                        l_round += lr;
+                        store_p(part);
+                        release_p(part);
+                    }
                 }
             } else {
+                float tile_ls = 0.f, tile_lr = 0.f;
                 uint32_t sr[32];
                 float mx = kNegInf;
 #pragma unroll 1
@@ -578,9 +744,12 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                 if (!edge) mx *= sl2;
                 const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
                 const bool moved = (m_new != m);
-                alpha = moved ? ex2(m - m_new) : 1.f;
+                const float alpha = moved ? ex2(m - m_new) : 1.f;
                 const float m_use = (m_new == kNegInf) ? 0.f : m_new;
-                if (j > 0 && __any_sync(0xffffffffu, moved)) rescale_o(alpha);
+                if (j > 0 && __any_sync(0xffffffffu, moved)) {
+                    o_settled(0);
+                    rescale_o(alpha);
+                }
                 m = m_new;
                 const uint64_t negm2 = f2_pack(-m_use, -m_use);
 #pragma unroll 1
@@ -597,12 +766,10 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                     tile_ls += s0 + s1;
                     tile_lr += t0 + t1;
                 }
+                l_exact = l_exact * alpha + tile_ls;
+                l_round = l_round * alpha + tile_lr;
+                release_p(0);
             }
-            l_exact = l_exact * alpha + tile_ls;
-            l_round = l_round * alpha + tile_lr;
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar(S::BAR_PFULL + q));
         }
 
         // ---------------- epilogue ----------------
@@ -610,13 +777,13 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
         // (unnormalised O, m, l_exact, l_round per row) in its own shared
         // memory; the first part merges them with its own, with the same
         // rescale as between tiles: M = max_p m_p, weights 2^(m_p - M).
-        if (nkv[q] > 0 && ok) ok = mbar_wait(bar(S::BAR_OFULL + q), 0, abort_flag, p.err, 21);
+        if (nkvq > 0 && ok) ok = mbar_wait(bar(S::BAR_OFULL + q), 0, abort_flag, p.err, 21);
         tc_fence_after();
         float a_own = 1.f;                 // weight of this CTA's O
         float a_part[8];                   // weights of the other parts' O
         float le_fin = l_exact, lr_fin = l_round, m_fin = m;
         bool write_out = true;
-        const uint32_t sPart = sRing;      // partials live in the (now idle) K/V ring
+        const uint32_t sPart = sQ;         // partials live in the (now idle) Q tiles and K/V ring
         const uint32_t part_row = sPart + ((q * 128 + row_in) * S::PSTR) * 4;
         auto stat_addr = [&](int k) { return sPart + (NQ * 128 * S::PSTR + k * NQ * 128 + q * 128 + row_in) * 4; };
 #pragma unroll
@@ -627,7 +794,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                 // tiles) has completed: the other tile's last PV may still read V.
                 mbar_wait(bar(S::BAR_DONE), 0, abort_flag, p.err, 24);
                 tc_fence_after();
-                if (nkv[q] > 0) {
+                if (nkvq > 0) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
@@ -652,7 +819,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                 mbar_wait_cluster(bar(S::BAR_PART), 0, abort_flag, p.err, 23);
                 float mp[8], lep[8], lrp[8];
                 m_fin = m;
-                for (int pp = 1; pp < nparts; ++pp) {
+#pragma unroll
+                for (int pp = 1; pp < 8; ++pp) {
+                    if (pp >= nparts) break;
                     mp[pp] = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
                     lep[pp] = ld_cluster_f32(mapa_shared(stat_addr(1), pp));
                     lrp[pp] = ld_cluster_f32(mapa_shared(stat_addr(2), pp));
@@ -666,7 +835,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                     a_own = (m == kNegInf) ? 0.f : ex2(m - m_fin);
                     le_fin = a_own * l_exact;
                     lr_fin = a_own * l_round;
-                    for (int pp = 1; pp < nparts; ++pp) {
+#pragma unroll
+                    for (int pp = 1; pp < 8; ++pp) {
+                        if (pp >= nparts) break;
                         a_part[pp] = (mp[pp] == kNegInf) ? 0.f : ex2(mp[pp] - m_fin);
                         le_fin += a_part[pp] * lep[pp];
                         lr_fin += a_part[pp] * lrp[pp];
@@ -674,7 +845,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                 }
             }
         }
-        if (nkv[q] > 0 && write_out) {
+        if (nkvq > 0 && write_out) {
             const bool any = (le_fin > 0.f) && (lr_fin > 0.f);
             const float inv = any ? 1.f / lr_fin : 0.f;
             const uint64_t inv2 = f2_pack(inv, inv);
@@ -691,7 +862,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                         // their shared memory through the cluster)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a_own);
-                        for (int pp = 1; pp < nparts; ++pp) {
+#pragma unroll
+                        for (int pp = 1; pp < 8; ++pp) {
+                            if (pp >= nparts) break;
                             if (a_part[pp] == 0.f) continue;
                             const uint32_t src = mapa_shared(part_row + 32 * c * 4, pp);
 #pragma unroll
@@ -732,7 +905,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             if (wq == 0 && lane == 0 && !*abort_flag) {
 #pragma unroll
                 for (int cb = 0; cb < S::CB; ++cb)
-                    tma_store_3d(&tm_o, stage + cb * (BR * 128), cb * 64, r0[q], bh);
+                    tma_store_3d(&tm_o, stage + cb * (BR * 128), cb * 64, r0q, bh);
                 tma_store_commit();
                 tma_store_wait_read0();
             }
@@ -794,7 +967,7 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
     if (attr_device != dev) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES) != cudaSuccess)
             return kErrCuda;
-        if (S::SPLIT_REGS) {
+        if (S::MOVE_REGS) {
             // setmaxnreg moves registers within the launch allocation; the split
             // above is exact only for this per-thread count.
             cudaFuncAttributes fa;
