@@ -10,39 +10,39 @@
 //
 // GB300 mapping: one CTA per group of NQ consecutive BR-row query tiles of one
 // (batch, head); heaviest groups (largest row index, for causal) launch first.
-//   warp 4*NQ      TMA producer: Q tiles once, then K_j / V_j tiles into a
+//   warps 0 .. 4*NQ*NH-1  softmax warpgroups: NH per query tile (NH = 2 for
+//                  BC = 128: each owns half of the tile's key columns and half
+//                  of O's columns).  One thread per row (tensor-memory lane =
+//                  row).  Reads its S columns, applies scale and masks, keeps
+//                  the row state (m, l), rescales its O columns in tensor
+//                  memory when needed, writes its part of P as bf16 back over
+//                  its S columns, then the epilogue (normalise, bf16, TMA
+//                  store; LSE).
+//   next warp      TMA producer: Q tiles once, then K_j / V_j tiles into a
 //                  ring of NS shared-memory slots (128-byte swizzle).
-//   warp 4*NQ + 1  MMA issuer (one thread): S_q = Q_q K_j^T (both operands in
-//                  shared memory) and O_q += P_q V_j (P from tensor memory, V
-//                  MN-major in shared memory) on tcgen05, f32 accumulators in
-//                  tensor memory.
-//   warps 4q..4q+3 softmax warpgroup of query tile q: one thread per row
-//                  (tensor-memory lane = row).  Reads S_q, applies scale and
-//                  masks, updates (m, l), rescales O_q in tensor memory when
-//                  needed, writes P_q as bf16 back over S_q's columns, then
-//                  the epilogue (normalise, bf16, TMA store; LSE).
-// The MMA issue order S_0(j+1) after PV_0(j), S_1(j+1) after PV_1(j) lets the
-// tensor pipe work on one tile while the other tile's softmax runs.  With
-// BC = 128 the softmax hands P over in two halves, so the first half's P V runs
-// while the second half is exponentiated.  With BC = 64 each query tile has
-// two S buffers in tensor memory and S_q(j+2) is issued right after P_q V_j, so
-// the softmax of one tile never waits for its own P V.  Where the 128-column
-// softmax needs more than the launch share of registers, setmaxnreg moves
-// registers from the producer/MMA warpgroup to the softmax warpgroups.
+//   next warp      MMA issuer (one elected lane): S_q = Q_q K_j^T (both
+//                  operands in shared memory) and O_q += P_q V_j (P from tensor
+//                  memory, V MN-major in shared memory) on tcgen05, f32
+//                  accumulators in tensor memory.
+// The MMA issue order S_0(j+1) after P_0 V_j, S_1(j+1) after P_1 V_j lets the
+// tensor pipe work on one tile while the other tile's softmax runs; each half
+// of P is handed over as soon as its warpgroup has written it.  Where tensor
+// memory has room (BC = 64) each query tile has two S buffers and S_q(j+2) is
+// issued right after P_q V_j, so the softmax never waits for its own P V.
 //
 // BR = 64 uses M = 64 MMAs, whose accumulator rows r sit in tensor-memory lane
 // 32*(r/16) + r%16: lanes 0..15 of each warp carry rows, lanes 16..31 idle.
 //
-// The reference maximum m is set from a row's first tile with an allowed key
-// (moved only if the tile maximum exceeds it by more than kRescaleThresh, log2
-// units).  Later tiles are exponentiated against m without computing their
-// maximum; only a tile whose p sum past kFastSumLimit = 2^16 moves m to its
-// maximum and is redone.  Exact up to rounding because a / l does not depend
-// on the reference point, and every p stays <= 2^16.
-// Two denominators are kept: the sum of the bf16-rounded p that actually
-// enter P V (normalises O, so the applied weights sum to one) and the float32
-// sum of p (gives the LSE).
+// The reference maximum m is set from a row's first tile.  Later tiles are
+// exponentiated against m without computing their maximum; only a tile whose
+// p sum passes kFastSumLimit = 2^16 (or that has no finite reference yet)
+// moves m to the row's maximum and is redone.  Exact up to rounding because
+// O / l does not depend on the reference point, and every p stays <= 2^16.
+// The two warpgroups of a tile take this decision together.
+// One denominator per row, the float32 sum of p: it normalises O (whose P V
+// uses p rounded to bf16) and gives the LSE.
 #include <cuda_bf16.h>
+#include <type_traits>
 #include <cstdio>
 
 #include "internal.h"
@@ -67,60 +67,64 @@ struct TcShape {
     static constexpr int SMEM_BUDGET = 225 * 1024;  // leaves room for barriers and alignment
     // key mask of the current tile in log2 units, double-buffered per query tile
     static constexpr int MASK_BYTES = MASKED ? NQ * 2 * BC * 4 : 0;
-    static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES - MASK_BYTES) / SLOT_BYTES;
-    static constexpr int NS = NS_RAW > 8 ? 8 : (NS_RAW < 2 ? 2 : NS_RAW);
-    // Two S buffers per query tile when tensor memory has room (BC = 64 with
-    // two query tiles): S_q(j+2) is computed while the softmax works on S_q(j+1)
-    // and P_q(j) waits for its P V, instead of after P V.
-    static constexpr bool DBS = (NQ == 2) && (2 * NQ * BC + NQ * D <= 512);
+    // Two S buffers per query tile when tensor memory has room: S_q(j+2) is
+    // computed while the softmax works on S_q(j+1) and P_q(j) waits for its
+    // P V, instead of after P V.
+    static constexpr bool DBS = 2 * NQ * BC + NQ * D <= 512;
     static constexpr int NSB = DBS ? 2 : 1;
-    // With one S buffer and BC = 128, P is handed to the MMA in two halves: the
-    // first half's P V runs while the softmax works on the second half.
-    static constexpr int NP = (!DBS && BC == 128) ? 2 : 1;
+    // BC = 128: two softmax warpgroups share each query tile, one per half of
+    // its columns (and of O's columns); each hands its half of P to the MMA as
+    // soon as it is written.
+    static constexpr int NH = BC == 128 ? 2 : 1;
+    // two warpgroups per tile exchange per-row values (half maxima, partial sums)
+    static constexpr int XCH_BYTES = NH == 2 ? NQ * 2 * 128 * 8 : 0;
+    static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES - MASK_BYTES - XCH_BYTES) / SLOT_BYTES;
+    static constexpr int NS = NS_RAW > 8 ? 8 : (NS_RAW < 2 ? 2 : NS_RAW);
     static constexpr int TMEM_USED = NQ * (NSB * BC + D);
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32
                                      : TMEM_USED <= 64 ? 64
                                      : TMEM_USED <= 128 ? 128
                                      : TMEM_USED <= 256 ? 256 : 512;
-    static constexpr int SOFTMAX_WARPS = 4 * NQ;
+    static constexpr int SOFTMAX_WARPS = 4 * NQ * NH;
     static constexpr int WARP_TMA = SOFTMAX_WARPS;
     static constexpr int WARP_MMA = SOFTMAX_WARPS + 1;
-    // Two query tiles: a third full warpgroup (TMA, MMA, 2 idle) so that
+    // Two query tiles: a full extra warpgroup (TMA, MMA, 2 idle) so that
     // setmaxnreg can move registers between whole warpgroups.
     static constexpr bool SPLIT_REGS = (NQ == 2);
-    // setmaxnreg moves registers from the producer/MMA warpgroup to the softmax
-    // warpgroups where the 128-column softmax does not fit the launch share
-    // (168) without spilling; where it does fit (and for BC = 64) the move
-    // would only make the MMA issuer spill.  Chosen per shape from ptxas's
-    // spill counts.
-    static constexpr bool MOVE_REGS = SPLIT_REGS && BC == 128 && !(D == 128 && BR == 128 && !MASKED);
-    static constexpr int THREADS = SPLIT_REGS ? 384 : 32 * (SOFTMAX_WARPS + 2);
-    static constexpr int LAUNCH_REGS = 168;          // 65536 / 384, rounded down to 8
-    static constexpr int REGS_SOFTMAX = 208;
-    static constexpr int REGS_OTHER = 88;            // 2*128*208 + 128*88 == 384*168
+
+    // setmaxnreg could move registers from the producer/MMA warpgroup to the
+    // softmax warpgroups; every shape here fits the launch share, and the
+    // move only makes ptxas spill around it.
+    static constexpr bool MOVE_REGS = false;
+    // softmax warps + TMA + MMA (a whole warpgroup for those two when
+    // registers are moved, since setmaxnreg acts per warpgroup)
+    static constexpr int THREADS = MOVE_REGS ? 32 * SOFTMAX_WARPS + 128 : 32 * (SOFTMAX_WARPS + 2);
+    static constexpr int LAUNCH_REGS = NH == 2 ? 96 : 168;   // 65536 / THREADS, rounded down to 8
+    static constexpr int REGS_SOFTMAX = NH == 2 ? 112 : 208;
+    static constexpr int REGS_OTHER = NH == 2 ? 32 : 88;     // softmax + other shares == THREADS * LAUNCH_REGS
     // shared memory layout (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * Q_BYTES;
     static constexpr int OFF_MASK = OFF_RING + NS * SLOT_BYTES;
-    static constexpr int OFF_BAR = OFF_MASK + MASK_BYTES;
-    // barriers: q_full[NQ] full[NS] empty[NS] s_full[NQ][NSB] p_full[NQ][NSB][NP] o_full[NQ]
+    static constexpr int OFF_XCH = OFF_MASK + MASK_BYTES;
+    static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
+    // barriers: q_full[NQ] full[NS] empty[NS] s_full[NQ][NSB] p_full[NQ][NSB][NH] o_full[NQ]
     // pv_done[NQ] done part done_read
     static constexpr int BAR_QFULL = 0;
     static constexpr int BAR_FULL = BAR_QFULL + NQ;
     static constexpr int BAR_EMPTY = BAR_FULL + NS;
     static constexpr int BAR_SFULL = BAR_EMPTY + NS;
     static constexpr int BAR_PFULL = BAR_SFULL + NQ * NSB;
-    static constexpr int BAR_OFULL = BAR_PFULL + NQ * NSB * NP;
-    // two S buffers: each P_q V has completed; P in two halves: the first half's P_q V has completed
-    static constexpr int BAR_PVDONE = BAR_OFULL + NQ;
+    static constexpr int BAR_OFULL = BAR_PFULL + NQ * NSB * NH;
+    static constexpr int BAR_PVDONE = BAR_OFULL + NQ;   // two S buffers: each P_q V has completed
     static constexpr int BAR_DONE = BAR_PVDONE + NQ;
     static constexpr int BAR_PART = BAR_DONE + 1;       // split K/V: partials of the other parts are ready
     static constexpr int BAR_DONEREAD = BAR_PART + 1;   // split K/V: the first part has read this one's partial
     static constexpr int NBARS = BAR_DONEREAD + 1;
     // split K/V: a part's partial results, staged in the (then idle) Q tiles and K/V ring:
-    // unnormalised O rows (float32, padded stride) and the per-row m, l_exact, l_round
+    // unnormalised O rows (float32, padded stride) and the per-row m, l
     static constexpr int PSTR = D + 4;
-    static constexpr int PART_BYTES = (NQ * 128 * PSTR + 3 * NQ * 128) * 4;
+    static constexpr int PART_BYTES = (NQ * 128 * PSTR + 2 * NQ * 128) * 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     // + alignment slack; a 512-column tensor-memory user also claims enough
     // shared memory that no second CTA can be resident (its allocation would wait)
@@ -137,7 +141,7 @@ struct TcShape {
     // A 512-column allocation must never wait for another resident CTA.
     static_assert(TMEM_COLS < 512 || SMEM_BYTES > 116 * 1024, "one CTA per SM for full TMEM");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-    static_assert(!MOVE_REGS || 2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER == THREADS * LAUNCH_REGS,
+    static_assert(!MOVE_REGS || 32 * SOFTMAX_WARPS * REGS_SOFTMAX + 128 * REGS_OTHER == THREADS * LAUNCH_REGS,
                   "register split must equal the launch allocation");
     // two S buffers: K_{j+2} is waited for while V_j still holds its slot
     static_assert(!DBS || NS >= 4, "ring depth for two S buffers");
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             mbar_init(bar(S::BAR_QFULL + q), 1);
             for (int b = 0; b < S::NSB; ++b) {
                 mbar_init(bar(S::BAR_SFULL + q * S::NSB + b), 1);
-                for (int h = 0; h < S::NP; ++h) mbar_init(bar(S::BAR_PFULL + (q * S::NSB + b) * S::NP + h), 128);
+                for (int h = 0; h < S::NH; ++h) mbar_init(bar(S::BAR_PFULL + (q * S::NSB + b) * S::NH + h), 128);
             }
             mbar_init(bar(S::BAR_OFULL + q), 1);
             mbar_init(bar(S::BAR_PVDONE + q), 1);
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             mbar_init(bar(S::BAR_EMPTY + s), 1);
         }
         mbar_init(bar(S::BAR_DONE), 1);
-        mbar_init(bar(S::BAR_PART), static_cast<uint32_t>((nparts > 1 ? nparts - 1 : 1) * NQ * 128));
+        mbar_init(bar(S::BAR_PART), static_cast<uint32_t>((nparts > 1 ? nparts - 1 : 1) * S::SOFTMAX_WARPS * 32));
         mbar_init(bar(S::BAR_DONEREAD), 1);
         *abort_flag = 0u;
         fence_mbar_init();
@@ -333,14 +337,16 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                     tc_commit(bar(S::BAR_SFULL + q * S::NSB + b));
                 }
             };
-            // P_q V_j over K steps [BC/16 * h / NP, BC/16 * (h+1) / NP): part h of P
+            // P_q V_j over K steps [BC/16 * h / NH, BC/16 * (h+1) / NH): half h of P,
+            // which its warpgroup wrote over the first columns of its half of S
+            constexpr int KPH = (BC / 16) / S::NH;   // K steps per half
             auto issue_pv = [&](int q, int j, int h) {
                 const int b = j & (S::NSB - 1);
                 const uint64_t b0 = vdesc0 + static_cast<uint64_t>((((2 * j + 1) % S::NS) * S::SLOT_BYTES) >> 4);
                 if (leader) {
 #pragma unroll
-                    for (int kk = (BC / 16) * h / S::NP; kk < (BC / 16) * (h + 1) / S::NP; ++kk) {
-                        mma_bf16_ts(tmem + S::o_col(q), tmem + S::s_col(q, b) + kk * 8,
+                    for (int kk = (BC / 16) * h / S::NH; kk < (BC / 16) * (h + 1) / S::NH; ++kk) {
+                        mma_bf16_ts(tmem + S::o_col(q), tmem + S::s_col(q, b) + (kk / KPH) * (BC / S::NH) + (kk % KPH) * 8,
                                     b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_o,
                                     (j > 0 || kk > 0) ? 1u : 0u);
                     }
@@ -374,12 +380,15 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                     bool k_ready = false;
                     for (int q = 0; q < NQ && ok; ++q) {
                         if (j >= nkv[q]) continue;
-                        if (!wwait(bar(S::BAR_PFULL + q * S::NSB + (j & 1)), (j >> 1) & 1, 13)) {
-                            ok = false;
-                            break;
+                        for (int h = 0; h < S::NH && ok; ++h) {
+                            if (!wwait(bar(S::BAR_PFULL + (q * S::NSB + (j & 1)) * S::NH + h), (j >> 1) & 1, 13)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_pv(q, j, h);
                         }
-                        tc_fence_after();
-                        issue_pv(q, j, 0);
+                        if (!ok) break;
                         commit(S::BAR_PVDONE + q);
                         if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
                         if (j + 2 < nkv[q]) {
@@ -415,14 +424,13 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                     const int tk = 2 * j + 2;
                     for (int q = 0; q < NQ && ok; ++q) {
                         if (j >= nkv[q]) continue;
-                        for (int h = 0; h < S::NP && ok; ++h) {
-                            if (!wwait(bar(S::BAR_PFULL + q * S::NP + h), j & 1, 13)) {
+                        for (int h = 0; h < S::NH && ok; ++h) {
+                            if (!wwait(bar(S::BAR_PFULL + q * S::NH + h), j & 1, 13)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
                             issue_pv(q, j, h);
-                            if (S::NP > 1 && h == 0) commit(S::BAR_PVDONE + q);
                         }
                         if (!ok) break;
                         if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
@@ -449,10 +457,14 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------------
-        // Softmax warpgroup of query tile q
+        // Softmax warpgroup h of query tile q.  NH = 2: warpgroup h owns S
+        // columns [BC/2*h, BC/2*(h+1)), the matching half of P (written over
+        // the first BC/4 of those columns) and half of O's columns; the two
+        // warpgroups of a tile agree on every row's reference maximum.
         // ------------------------------------------------------------------
         if constexpr (S::MOVE_REGS) regs_inc<S::REGS_SOFTMAX>();
-        const int q = warp >> 2;
+        const int q = warp / (4 * S::NH);
+        const int h = (warp >> 2) & (S::NH - 1);
         const int wq = warp & 3;
         // This tile's row offset and K/V tile count as plain registers (a
         // run-time index into r0[] / nkv[] would place them in local memory).
@@ -472,17 +484,29 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
         const uint32_t tO = tmem + t_lane + S::o_col(q);
         const float sl2 = p.scale_log2;
         const float *mrow = MASKED ? p.key_mask + static_cast<size_t>(bh) * N : nullptr;
-        float m = kNegInf;    // reference maximum, log2 units
-        float l_exact = 0.f;  // sum of float32 p (for LSE)
-        float l_round = 0.f;  // sum of the bf16-rounded p used in P V (normalises O)
+        constexpr int CW = BC / S::NH;       // S columns of this warpgroup
+        constexpr int OC = D / 32 / S::NH;   // 32-column chunks of O of this warpgroup
+        float m = kNegInf;    // reference maximum, log2 units (the same in both warpgroups)
+        float l = 0.f;        // sum of float32 p over this warpgroup's columns
         bool ok = true;
+        // per-row exchange slot of warpgroup hh of this tile; barrier of the pair
+        auto xch = [&](int hh) -> uint32_t { return sbase + S::OFF_XCH + ((q * 2 + hh) * 128 + row_in) * 8; };
+        auto pair_sync = [&]() { named_bar_sync(7 + q, 256); };
+        // (a, b) of this row from the other warpgroup, after publishing our own
+        // (M = 64: only the lane that carries the row writes its slot)
+        auto exchange = [&](float a, float b, float &ao, float &bo) {
+            if (active) asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(xch(h)), "f"(a), "f"(b) : "memory");
+            pair_sync();
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(ao), "=f"(bo) : "r"(xch(1 - h)) : "memory");
+        };
 
+        // A wait that gives up (the error word records it; every later wait
+        // then gives up at once) does not end the loop: the tile is computed
+        // from whatever tensor memory holds, so every warp still takes part in
+        // every named barrier of the loop and no partner is left waiting.
         for (int j = 0; j < nkvq; ++j) {
             const int sb = j & (S::NSB - 1);   // S buffer of this tile
-            if (!mbar_wait(bar(S::BAR_SFULL + q * S::NSB + sb), (j / S::NSB) & 1, abort_flag, p.err, 20)) {
-                ok = false;
-                break;
-            }
+            if (!mbar_wait(bar(S::BAR_SFULL + q * S::NSB + sb), (j / S::NSB) & 1, abort_flag, p.err, 20)) ok = false;
             tc_fence_after();
             const uint32_t tS = tmem + t_lane + S::s_col(q, sb);
             const int key0 = (kv_lo + j) * BC;
@@ -491,17 +515,17 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             const bool edge = MASKED || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0q);
 
             const bool diag = p.causal && key0 + BC - 1 > r0q;   // tile crosses the causal diagonal
-            // Key mask of this tile, once per warpgroup, in log2 units with -inf
+            // Key mask of this warpgroup's columns, in log2 units with -inf
             // past N; double-buffered so one barrier per tile suffices.
             const float *msm = reinterpret_cast<const float *>(smem + S::OFF_MASK) + (q * 2 + (j & 1)) * BC;
             if constexpr (MASKED) {
                 float *mw = reinterpret_cast<float *>(smem + S::OFF_MASK) + (q * 2 + (j & 1)) * BC;
 #pragma unroll
-                for (int t = row_in; t < BC; t += 128) {
+                for (int t = h * CW + row_in; t < (h + 1) * CW; t += 128) {
                     const int key = key0 + t;
                     mw[t] = (key < N) ? __ldg(mrow + key) * kLog2e : kNegInf;
                 }
-                named_bar_sync(3 + q, 128);
+                named_bar_sync(3 + q * S::NH + h, 128);
             }
             // One loaded 32-column chunk -> log2-domain scores
             // x = s*scale*log2(e) (+ mask*log2(e)), -inf where not allowed.
@@ -528,8 +552,8 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             // over S's first BC/2 columns (chunk c -> columns 16c .. 16c+15,
             // never ahead of the chunks still to be read).
             // Partial sums per chunk keep the add chains short: ls2 sums the
-            // float32 p, lr2 the bf16-rounded p (both as float32 pairs).
-            auto exp_chunk = [&](int c, const uint32_t *r, uint64_t negm2, uint64_t &ls2, uint64_t &lr2) {
+            // float32 p as float32 pairs.
+            auto exp_chunk = [&](int c, const uint32_t *r, uint64_t negm2, uint64_t &ls2) {
                 const uint64_t sl2x2 = f2_pack(sl2, sl2);
                 uint32_t pk[16];
 #pragma unroll
@@ -543,17 +567,16 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                     if (!active) w = 0u;
                     pk[e] = w;
                     ls2 = f2_add(ls2, f2_pack(p0, p1));
-                    lr2 = f2_add(lr2, f2_pack(bf16lo_to_f32(w), bf16hi_to_f32(w)));
                 }
                 tmem_st16(tS + 16 * c, pk);
             };
 
-            // O_q *= alpha for this warp's rows (warp-collective; alpha = 1 for
-            // rows whose reference did not move).
+            // O_q *= alpha for this warp's rows and this warpgroup's columns
+            // (warp-collective; alpha = 1 for rows whose reference did not move).
             auto rescale_o = [&](float alpha) {
                 const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = h * OC; c < (h + 1) * OC; ++c) {
                     uint32_t o[32];
                     tmem_ld32(tO + 32 * c, o);
                     tmem_ld_wait();
@@ -571,75 +594,70 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             };
 
             constexpr bool kTwoPass = BC > 128;   // 256 columns do not fit in registers
-            // Before O_q is rescaled it must hold every P V issued so far: the
-            // one of tile j-1 may still run with two S buffers, and the first
-            // half of this tile's P may be in flight once handed over.
-            auto o_settled = [&](int part) {
+            // With two S buffers the P V of tile j-1 may still run: O_q holds
+            // it only after that P V has completed.
+            auto o_settled = [&]() {
                 if constexpr (S::DBS) {
                     mbar_wait(bar(S::BAR_PVDONE + q), (j - 1) & 1, abort_flag, p.err, 25);
                     tc_fence_after();
-                } else if constexpr (S::NP > 1) {
-                    if (part > 0) {
-                        mbar_wait(bar(S::BAR_PVDONE + q), j & 1, abort_flag, p.err, 25);
-                        tc_fence_after();
-                    }
                 }
             };
-            // Part `part` of P_q is in tensor memory: its P V may be issued.
-            auto release_p = [&](int part) {
+            // This warpgroup's part of P_q is in tensor memory: its P V may be issued.
+            auto release_p = [&]() {
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(bar(S::BAR_PFULL + (q * S::NSB + sb) * S::NP + part));
+                mbar_arrive(bar(S::BAR_PFULL + (q * S::NSB + sb) * S::NH + h));
             };
             if constexpr (!kTwoPass) {
-                // S is read from tensor memory in groups of HC columns; the load
-                // of the next group is in flight while one is exponentiated.
-                constexpr int HC = BC < 64 ? BC : 64;
-                constexpr int NG = BC / HC;
-                constexpr int GPP = NG / S::NP;     // groups per part of P
-                static_assert(NG % S::NP == 0, "parts of P");
-                uint32_t pk[BC / 2];
+                // This warpgroup's S columns are read from tensor memory in
+                // groups of HC; the load of the next group is in flight while
+                // one is exponentiated.
+                constexpr int HC = CW < 64 ? CW : 64;
+                constexpr int NG = CW / HC;
+                uint32_t pk[CW / 2];
                 auto issue_group = [&](int g, uint32_t *sr) {
 #pragma unroll
-                    for (int c = 0; c < HC / 32; ++c) tmem_ld32(tS + HC * g + 32 * c, sr + 32 * c);
+                    for (int c = 0; c < HC / 32; ++c) tmem_ld32(tS + h * CW + HC * g + 32 * c, sr + 32 * c);
                 };
-                // after the wait: scale/masks where needed
-                auto finish_group = [&](int g, uint32_t *sr) {
+                // after the wait: scale/masks where needed (EDGE: this tile needs them)
+                auto finish_group = [&](auto edge_c, int g, uint32_t *sr) {
 #pragma unroll
                     for (int c = 0; c < HC / 32; ++c) reg_fence32(sr + 32 * c);
-                    if (edge) {
+                    if constexpr (decltype(edge_c)::value) {
 #pragma unroll
-                        for (int c = 0; c < HC / 32; ++c) mask_chunk((HC / 32) * g + c, sr + 32 * c);
+                        for (int c = 0; c < HC / 32; ++c) mask_chunk((h * CW + HC * g) / 32 + c, sr + 32 * c);
                     }
                 };
-                auto load_group = [&](int g, uint32_t *sr) {
+                auto load_group = [&](auto edge_c, int g, uint32_t *sr) {
                     issue_group(g, sr);
                     tmem_ld_wait();
-                    finish_group(g, sr);
+                    finish_group(edge_c, g, sr);
                 };
-                // p = 2^(x - m_use) for the columns of one part of P into pk
-                // (bf16 pairs) and the part's two sums.
-                auto exps = [&](int part, float m_use, float &ls, float &lr) {
+                // p = 2^(x - m_use) over this warpgroup's columns into pk (bf16
+                // pairs) and their sum; the tile's kind (edge or not) is a
+                // compile-time branch so the inner loop carries no select.
+                auto exps_k = [&](auto edge_c, float m_use, float &ls) {
+                    constexpr bool EDGE = decltype(edge_c)::value;
                     const uint64_t negm2 = f2_pack(-m_use, -m_use);
                     const uint64_t sl2x2 = f2_pack(sl2, sl2);
                     ls = 0.f;
-                    lr = 0.f;
                     uint32_t sbuf[2][HC];
-                    load_group(part * GPP, sbuf[0]);
+                    load_group(edge_c, 0, sbuf[0]);
 #pragma unroll
-                    for (int gi = 0; gi < GPP; ++gi) {
-                        const int g = part * GPP + gi;
-                        uint32_t *sr = sbuf[gi & 1];
-                        if (gi + 1 < GPP) issue_group(g + 1, sbuf[(gi + 1) & 1]);
+                    for (int g = 0; g < NG; ++g) {
+                        uint32_t *sr = sbuf[g & 1];
+                        if (g + 1 < NG) issue_group(g + 1, sbuf[(g + 1) & 1]);
 #pragma unroll
                         for (int c = 0; c < HC / 32; ++c) {
-                            uint64_t ls2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
+                            uint64_t ls2 = f2_pack(0.f, 0.f);
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const float x0 = __uint_as_float(sr[32 * c + 2 * e]);
                                 const float x1 = __uint_as_float(sr[32 * c + 2 * e + 1]);
                                 const uint64_t xx = f2_pack(x0, x1);
-                                const uint64_t y = edge ? f2_add(xx, negm2) : f2_fma(xx, sl2x2, negm2);
+                                uint64_t y;
+                                if constexpr (EDGE) y = f2_add(xx, negm2);
+                                else y = f2_fma(xx, sl2x2, negm2);
                                 float y0, y1;
                                 f2_unpack(y, y0, y1);
                                 const float p0 = ex2(y0), p1 = ex2(y1);
@@ -647,90 +665,76 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                                 if (!active) w = 0u;
                                 pk[(HC / 2) * g + 16 * c + e] = w;
                                 ls2 = f2_add(ls2, f2_pack(p0, p1));
-                                lr2 = f2_add(lr2, f2_pack(bf16lo_to_f32(w), bf16hi_to_f32(w)));
                             }
-                            float s0, s1, t0, t1;
+                            float s0, s1;
                             f2_unpack(ls2, s0, s1);
-                            f2_unpack(lr2, t0, t1);
                             ls += s0 + s1;
-                            lr += t0 + t1;
                         }
-                        if (gi + 1 < GPP) {
+                        if (g + 1 < NG) {
                             tmem_ld_wait();
-                            finish_group(g + 1, sbuf[(gi + 1) & 1]);
+                            finish_group(edge_c, g + 1, sbuf[(g + 1) & 1]);
                         }
                     }
                 };
-                // P chunk c (32 keys) -> S columns 16c .. 16c+15
-                auto store_p = [&](int part) {
-#pragma unroll
-                    for (int c = part * (BC / 32 / S::NP); c < (part + 1) * (BC / 32 / S::NP); ++c)
-                        tmem_st16(tS + 16 * c, pk + 16 * c);
+                auto exps = [&](float m_use, float &ls) {
+                    if (edge) exps_k(std::true_type{}, m_use, ls);
+                    else exps_k(std::false_type{}, m_use, ls);
                 };
-                // maximum over the columns of parts [p0, p1)
-                auto parts_max = [&](int p0, int p1) {
+                // P chunk c (32 keys) of this warpgroup -> its S columns 16c .. 16c+15
+                auto store_p = [&]() {
+#pragma unroll
+                    for (int c = 0; c < CW / 32; ++c) tmem_st16(tS + h * CW + 16 * c, pk + 16 * c);
+                };
+                auto cols_max = [&]() {
                     float mx = kNegInf;
 #pragma unroll
-                    for (int g = p0 * GPP; g < p1 * GPP; ++g) {
+                    for (int g = 0; g < NG; ++g) {
                         uint32_t sr[HC];
-                        load_group(g, sr);
+                        load_group(std::true_type{}, g, sr);   // scaled and masked: max in log2 units
 #pragma unroll
                         for (int c = 0; c < HC / 32; ++c) mx = chunk_max(sr + 32 * c, mx);
                     }
-                    return edge ? mx : mx * sl2;   // scale > 0: max commutes with the scaling
+                    return mx;
                 };
-                if (__all_sync(0xffffffffu, !active || m != kNegInf)) {
-                    // Every row has a finite reference: exponentiate against it
-                    // with no maximum.  A row whose part sum exceeds
-                    // kFastSumLimit (or overflows) has a score far past the
-                    // reference: only then is the part's maximum taken and the
-                    // part redone (its S columns are still intact; its P is
-                    // written after).  Each part of P is released as it is done.
-#pragma unroll
-                    for (int part = 0; part < S::NP; ++part) {
-                        float ls, lr, a = 1.f;
-                        exps(part, m, ls, lr);
-                        const bool need = active && !(ls <= kFastSumLimit);
-                        if (__any_sync(0xffffffffu, need)) {
-                            const float mx = parts_max(part, part + 1);
-                            const float m_new = need ? fmaxf(mx, m) : m;
-                            a = need ? ex2(m - m_new) : 1.f;
-                            o_settled(part);
-                            rescale_o(a);   // j > 0 here: a finite reference needs an earlier tile
-                            m = m_new;
-                            exps(part, m, ls, lr);
-                        }
-                        l_exact = l_exact * a + ls;
-                        l_round = l_round * a + lr;
-                        store_p(part);
-                        release_p(part);
+                // Exponentiate against the current reference with no maximum.
+                // A row whose sum exceeds kFastSumLimit (or overflows, or has
+                // no finite reference yet) has a score far past the reference:
+                // only then is the tile's maximum taken, the reference moved
+                // and the tile redone (S is still intact: P is written after).
+                // The first tile of a row has no reference: maximum first.
+                float ls = 0.f;
+                bool need = active;
+                if (j > 0) {
+                    exps(m, ls);
+                    need = active && !(ls <= kFastSumLimit);
+                }
+                bool redo;
+                if constexpr (S::NH == 2) redo = named_bar_red_or(7 + q, 256, need);
+                else redo = __any_sync(0xffffffffu, need);
+                if (redo) {
+                    float mx = cols_max();
+                    bool need_row = need;
+                    if constexpr (S::NH == 2) {
+                        float mo, no;
+                        exchange(mx, need ? 1.f : 0.f, mo, no);
+                        mx = fmaxf(mx, mo);
+                        need_row = need || (no != 0.f);
                     }
-                } else {
-                    // Maximum first: a row's first tile, or rows with no allowed
-                    // key so far.  p <= 2^kRescaleThresh afterwards: no redo.
-                    const float mx = parts_max(0, S::NP);
-                    const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
-                    const bool moved = (m_new != m);
-                    const float a = moved ? ex2(m - m_new) : 1.f;
-                    if (j > 0 && __any_sync(0xffffffffu, moved)) {
-                        o_settled(0);
+                    const float m_new = need_row ? fmaxf(m, mx) : m;
+                    const float a = (m_new == m) ? 1.f : ex2(m - m_new);   // m = -inf: nothing to scale
+                    if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+                        o_settled();
                         rescale_o(a);
                     }
                     m = m_new;
-                    l_exact *= a;
-                    l_round *= a;
-#pragma unroll
-                    for (int part = 0; part < S::NP; ++part) {
-                        float ls, lr;
-                        exps(part, m == kNegInf ? 0.f : m, ls, lr);
-                        l_exact += ls;
-                        l_round += lr;
-                        store_p(part);
-                        release_p(part);
-                    }
+                    l *= a;
+                    exps(m == kNegInf ? 0.f : m, ls);
                 }
+                l += ls;
+                store_p();
+                release_p();
             } else {
-                float tile_ls = 0.f, tile_lr = 0.f;
+                float tile_ls = 0.f;
                 uint32_t sr[32];
                 float mx = kNegInf;
 #pragma unroll 1
@@ -747,7 +751,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                 const float alpha = moved ? ex2(m - m_new) : 1.f;
                 const float m_use = (m_new == kNegInf) ? 0.f : m_new;
                 if (j > 0 && __any_sync(0xffffffffu, moved)) {
-                    o_settled(0);
+                    o_settled();
                     rescale_o(alpha);
                 }
                 m = m_new;
@@ -758,30 +762,34 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                     tmem_ld_wait();
                     reg_fence32(sr);
                     if (edge) mask_chunk(c, sr);
-                    uint64_t ls2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
-                    exp_chunk(c, sr, negm2, ls2, lr2);
-                    float s0, s1, t0, t1;
+                    uint64_t ls2 = f2_pack(0.f, 0.f);
+                    exp_chunk(c, sr, negm2, ls2);
+                    float s0, s1;
                     f2_unpack(ls2, s0, s1);
-                    f2_unpack(lr2, t0, t1);
                     tile_ls += s0 + s1;
-                    tile_lr += t0 + t1;
                 }
-                l_exact = l_exact * alpha + tile_ls;
-                l_round = l_round * alpha + tile_lr;
-                release_p(0);
+                l = l * alpha + tile_ls;
+                release_p();
             }
         }
 
         // ---------------- epilogue ----------------
+        // Two warpgroups per tile: each row's sum over all columns.
+        if constexpr (S::NH == 2) {
+            float lo, unused;
+            pair_sync();   // the other warpgroup has read the last tile's exchange
+            exchange(l, 0.f, lo, unused);
+            l += lo;
+        }
         // A split item: every part but the first publishes its partial result
-        // (unnormalised O, m, l_exact, l_round per row) in its own shared
+        // (unnormalised O, m, l per row) in its own shared
         // memory; the first part merges them with its own, with the same
         // rescale as between tiles: M = max_p m_p, weights 2^(m_p - M).
         if (nkvq > 0 && ok) ok = mbar_wait(bar(S::BAR_OFULL + q), 0, abort_flag, p.err, 21);
         tc_fence_after();
         float a_own = 1.f;                 // weight of this CTA's O
         float a_part[8];                   // weights of the other parts' O
-        float le_fin = l_exact, lr_fin = l_round, m_fin = m;
+        float l_fin = l, m_fin = m;
         bool write_out = true;
         const uint32_t sPart = sQ;         // partials live in the (now idle) Q tiles and K/V ring
         const uint32_t part_row = sPart + ((q * 128 + row_in) * S::PSTR) * 4;
@@ -796,7 +804,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                 tc_fence_after();
                 if (nkvq > 0) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = h * OC; c < (h + 1) * OC; ++c) {
                         uint32_t o[32];
                         tmem_ld32(tO + 32 * c, o);
                         tmem_ld_wait();
@@ -808,50 +816,47 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                                          : "memory");
                     }
                 }
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(0)), "f"(m) : "memory");
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(1)), "f"(l_exact) : "memory");
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(2)), "f"(l_round) : "memory");
+                if (h == 0) {
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(0)), "f"(m) : "memory");
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(1)), "f"(l) : "memory");
+                }
                 mbar_arrive_remote(mapa_shared(bar(S::BAR_PART), 0));
                 // this CTA's shared memory must outlive the first part's reads
                 mbar_wait_cluster(bar(S::BAR_DONEREAD), 0, abort_flag, p.err, 22);
                 write_out = false;
             } else if (nparts > 1) {
                 mbar_wait_cluster(bar(S::BAR_PART), 0, abort_flag, p.err, 23);
-                float mp[8], lep[8], lrp[8];
+                float mp[8], lp[8];
                 m_fin = m;
 #pragma unroll
                 for (int pp = 1; pp < 8; ++pp) {
                     if (pp >= nparts) break;
                     mp[pp] = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
-                    lep[pp] = ld_cluster_f32(mapa_shared(stat_addr(1), pp));
-                    lrp[pp] = ld_cluster_f32(mapa_shared(stat_addr(2), pp));
+                    lp[pp] = ld_cluster_f32(mapa_shared(stat_addr(1), pp));
                     m_fin = fmaxf(m_fin, mp[pp]);
                 }
                 if (m_fin == kNegInf) {
                     a_own = 0.f;
-                    le_fin = 0.f;
-                    lr_fin = 0.f;
+                    l_fin = 0.f;
                 } else {
                     a_own = (m == kNegInf) ? 0.f : ex2(m - m_fin);
-                    le_fin = a_own * l_exact;
-                    lr_fin = a_own * l_round;
+                    l_fin = a_own * l;
 #pragma unroll
                     for (int pp = 1; pp < 8; ++pp) {
                         if (pp >= nparts) break;
                         a_part[pp] = (mp[pp] == kNegInf) ? 0.f : ex2(mp[pp] - m_fin);
-                        le_fin += a_part[pp] * lep[pp];
-                        lr_fin += a_part[pp] * lrp[pp];
+                        l_fin += a_part[pp] * lp[pp];
                     }
                 }
             }
         }
         if (nkvq > 0 && write_out) {
-            const bool any = (le_fin > 0.f) && (lr_fin > 0.f);
-            const float inv = any ? 1.f / lr_fin : 0.f;
+            const bool any = l_fin > 0.f;
+            const float inv = any ? 1.f / l_fin : 0.f;
             const uint64_t inv2 = f2_pack(inv, inv);
             const uint32_t stage = sQ + q * S::Q_BYTES;  // Q_q is no longer read
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = h * OC; c < (h + 1) * OC; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tO + 32 * c, o);
                 tmem_ld_wait();
@@ -901,23 +906,23 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                 }
             }
             fence_proxy_async_smem();
-            named_bar_sync(1 + q, 128);
-            if (wq == 0 && lane == 0 && !*abort_flag) {
+            named_bar_sync(1 + q, 128 * S::NH);
+            if (h == 0 && wq == 0 && lane == 0 && !*abort_flag) {
 #pragma unroll
                 for (int cb = 0; cb < S::CB; ++cb)
                     tma_store_3d(&tm_o, stage + cb * (BR * 128), cb * 64, r0q, bh);
                 tma_store_commit();
                 tma_store_wait_read0();
             }
-            if (active && p.lse != nullptr && row < N) {
-                p.lse[static_cast<size_t>(bh) * N + row] = any ? (m_fin + log2f(le_fin)) * kLn2 : kNegInf;
+            if (h == 0 && active && p.lse != nullptr && row < N) {
+                p.lse[static_cast<size_t>(bh) * N + row] = any ? (m_fin + log2f(l_fin)) * kLn2 : kNegInf;
             }
         }
         if constexpr (S::CAN_SPLIT) {
             if (nparts > 1 && part == 0) {
                 // every softmax thread of the first part has read the other
                 // parts' shared memory: they may exit
-                named_bar_sync(5, NQ * 128);
+                named_bar_sync(9, S::SOFTMAX_WARPS * 32);
                 if (threadIdx.x == 0)
                     for (int pp = 1; pp < nparts; ++pp) mbar_arrive_remote(mapa_shared(bar(S::BAR_DONEREAD), pp));
             }

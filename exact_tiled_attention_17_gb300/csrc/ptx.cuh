@@ -171,6 +171,21 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Named barrier that also returns the OR of `pred` over the nthreads threads.
+__device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n"
+        "  .reg .pred pi, po;\n"
+        "  setp.ne.u32 pi, %1, 0;\n"
+        "  bar.red.or.pred po, %2, %3, pi;\n"
+        "  selp.u32 %0, 1, 0, po;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0u;
+}
 
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), 3-D tiled, no multicast
