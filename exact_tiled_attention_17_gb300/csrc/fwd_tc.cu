@@ -685,14 +685,17 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < CW / 32; ++c) tmem_st16(tS + h * CW + 16 * c, pk + 16 * c);
                 };
+                // maximum over this warpgroup's columns, 32 at a time (log2 units)
                 auto cols_max = [&]() {
                     float mx = kNegInf;
 #pragma unroll
-                    for (int g = 0; g < NG; ++g) {
-                        uint32_t sr[HC];
-                        load_group(std::true_type{}, g, sr);   // scaled and masked: max in log2 units
-#pragma unroll
-                        for (int c = 0; c < HC / 32; ++c) mx = chunk_max(sr + 32 * c, mx);
+                    for (int c = 0; c < CW / 32; ++c) {
+                        uint32_t sr[32];
+                        tmem_ld32(tS + h * CW + 32 * c, sr);
+                        tmem_ld_wait();
+                        reg_fence32(sr);
+                        mask_chunk(h * CW / 32 + c, sr);
+                        mx = chunk_max(sr, mx);
                     }
                     return mx;
                 };
@@ -729,10 +732,16 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                     m = m_new;
                     l *= a;
                     exps(m == kNegInf ? 0.f : m, ls);
+                    // P is stored in each branch: a shared store after the
+                    // branch would keep the first pass's P live through this one
+                    l += ls;
+                    store_p();
+                    release_p();
+                } else {
+                    l += ls;
+                    store_p();
+                    release_p();
                 }
-                l += ls;
-                store_p();
-                release_p();
             } else {
                 float tile_ls = 0.f;
                 uint32_t sr[32];
