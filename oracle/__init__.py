@@ -20,6 +20,14 @@ blocked_row(scores, values, width, block_order=None, no_rescale=False)
 deviation(a, b)
     Max-abs difference, 1-D Wasserstein-1 via sorting, mean/std of |a-b| and
     the signed mean (the paper's §IV-A and §V measures).
+round_fmt(x, mbits, ebits)
+    Rounding of binary64 values to an IEEE-style format with ``mbits``
+    fraction and ``ebits`` exponent bits (round to nearest even, subnormals,
+    overflow to infinity), from the definition (``oracle_emul.c``).
+emul(q, k, v, causal, scale, algo, Bc, mbits, ebits, key_mask=None, rows=None)
+    The paper's numerical re-implementation (§III, §IV-A Fig. 3): baseline
+    (algo 0) or tiled (algo 1, key blocks of width Bc) attention with every
+    tensor operation's result rounded to that format (``oracle_emul.c``).
 """
 from __future__ import annotations
 
@@ -32,6 +40,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle_attn.c")
+_SRC_EMUL = os.path.join(_HERE, "oracle_emul.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -40,12 +49,13 @@ ORACLE_NO_RESCALE = 1
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle_attn.c into liboracle.so next to it (gcc, -O2, no fast-math)."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+    """Compile oracle_attn.c and oracle_emul.c into liboracle.so next to them (gcc, -O2, no fast-math)."""
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_EMUL))
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= newest:
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fno-fast-math", "-fPIC", "-shared",
-           "-o", tmp, _SRC, "-lm", "-lpthread"]
+           "-o", tmp, _SRC, _SRC_EMUL, "-lm", "-lpthread"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -68,6 +78,13 @@ def _load():
             lib.oracle_blocked_row_f64.restype = ctypes.c_int
             lib.oracle_deviation_f64.argtypes = [dp, dp, ctypes.c_longlong, dp]
             lib.oracle_deviation_f64.restype = ctypes.c_int
+            lib.oracle_round_array.argtypes = [dp, dp, ctypes.c_longlong, ctypes.c_int, ctypes.c_int]
+            lib.oracle_round_array.restype = None
+            lib.oracle_emul_rows.argtypes = [dp, dp, dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, lp, ctypes.c_longlong, dp,
+                                             ctypes.c_int]
+            lib.oracle_emul_rows.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -169,3 +186,47 @@ def deviation(a, b) -> dict:
         raise RuntimeError("oracle_deviation_f64 failed")
     return {"max_abs": out[0], "w1": out[1], "mean_abs": out[2], "std_abs": out[3],
             "mean_signed": out[4], "n": int(A.size)}
+
+
+# Number formats of the precision sweep (fraction bits, exponent bits).
+FORMATS = {"bf16": (7, 8), "fp16": (10, 5), "tf32": (10, 8), "fp32": (23, 8), "fp64": (52, 11)}
+
+
+def round_fmt(x, mbits: int, ebits: int) -> np.ndarray:
+    """fl(x) in the format with ``mbits`` fraction and ``ebits`` exponent bits."""
+    lib = _load()
+    X = _f64(x)
+    Y = np.empty_like(X)
+    lib.oracle_round_array(_ptr(X), _ptr(Y), X.size, int(mbits), int(ebits))
+    return Y
+
+
+def emul(q, k, v, causal: bool, scale: float, algo: int, Bc: int, mbits: int, ebits: int,
+         key_mask=None, rows=None, nthreads: int | None = None) -> np.ndarray:
+    """Attention with every tensor op rounded to a format (see oracle_emul.c).
+
+    algo 0: baseline (softmax, then P V); algo 1: tiled online merge over key
+    blocks of width Bc.  Returns O [..., N, d] for all rows, or [nrows, d].
+    """
+    lib = _load()
+    Q, K, V = _f64(q), _f64(k), _f64(v)
+    if Q.shape != K.shape or Q.shape != V.shape or Q.ndim < 2:
+        raise ValueError("q, k, v must share one shape [..., N, d]")
+    lead = Q.shape[:-2]
+    N, d = Q.shape[-2], Q.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    M = None
+    if key_mask is not None:
+        M = _f64(key_mask)
+        if M.size != BH * N:
+            raise ValueError("key_mask must have BH*N elements")
+    R = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    nrows = BH * N if R is None else R.size
+    O = np.zeros((nrows, d), dtype=np.float64)
+    rc = lib.oracle_emul_rows(_ptr(Q), _ptr(K), _ptr(V), _ptr(M) if M is not None else None, BH, N, d,
+                              1 if causal else 0, float(scale), int(algo), int(Bc), int(mbits), int(ebits),
+                              _ptr(R, ctypes.c_longlong) if R is not None else None, nrows, _ptr(O),
+                              nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_emul_rows failed")
+    return O.reshape(*lead, N, d) if R is None else O

@@ -1,0 +1,132 @@
+"""Pins of the oracle's number-format emulation (CPU only).
+
+The emulation restates the paper's numerical re-implementation ("Is Flash
+Attention Stable?" §III, §IV-A Fig. 3): attention with every tensor
+operation's result rounded to a chosen format.  It is pinned here against
+things it does not compute itself:
+
+- its rounding function against the IEEE conversions numpy and torch perform
+  (binary32, binary16, bfloat16), including ties, subnormals and overflow;
+- at binary64 both emulated algorithms against the direct FP64 definition of
+  attention (``oracle.attn``), for every key-block width;
+- the trend the paper reports in Fig. 3: the FlashAttention-vs-baseline
+  deviation shrinks as the format's fraction bits grow.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _wide_values(rng, n, lo, hi):
+    """Random doubles with binary exponents spread over [lo, hi)."""
+    e = rng.uniform(lo, hi, n)
+    return np.where(rng.random(n) < 0.5, -1.0, 1.0) * np.exp2(e)
+
+
+def test_round_fp32_matches_ieee_conversion():
+    rng = np.random.default_rng(1)
+    x = _wide_values(rng, 20000, -160, 130)   # subnormal float32 .. overflow
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float32).astype(np.float64)
+    got = oracle.round_fmt(x, 23, 8)
+    assert np.array_equal(got, want)
+
+
+def test_round_fp32_ties_go_to_even():
+    rng = np.random.default_rng(2)
+    f = rng.standard_normal(5000).astype(np.float32)
+    nxt = np.nextafter(f, np.float32(np.inf))
+    mid = (f.astype(np.float64) + nxt.astype(np.float64)) / 2.0   # exact in binary64
+    want = mid.astype(np.float32).astype(np.float64)
+    assert np.array_equal(oracle.round_fmt(mid, 23, 8), want)
+    # the even neighbour wins: its last fraction bit is 0
+    bits = want.astype(np.float32).view(np.uint32)
+    assert np.all(bits & 1 == 0)
+
+
+def test_round_fp16_matches_ieee_conversion():
+    rng = np.random.default_rng(3)
+    x = _wide_values(rng, 20000, -28, 18)     # binary16 subnormals .. overflow
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).astype(np.float64)
+    got = oracle.round_fmt(x, 10, 5)
+    assert np.array_equal(got, want)
+    assert oracle.round_fmt(np.array([65519.0, 65520.0]), 10, 5).tolist() == [65504.0, math.inf]
+
+
+def test_round_bf16_matches_torch_conversion():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(4)
+    x32 = _wide_values(rng, 20000, -140, 127).astype(np.float32)
+    want = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_fmt(x32.astype(np.float64), 7, 8)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp16", "tf32", "fp32"])
+def test_round_is_idempotent_odd_and_monotone(fmt):
+    mb, eb = oracle.FORMATS[fmt]
+    emax = 2 ** (eb - 1) - 1
+    rng = np.random.default_rng(5)
+    x = np.sort(_wide_values(rng, 4000, max(-20, 1 - emax), min(20, emax)))   # normal range
+    y = oracle.round_fmt(x, mb, eb)
+    assert np.array_equal(oracle.round_fmt(y, mb, eb), y)
+    assert np.array_equal(oracle.round_fmt(-x, mb, eb), -y)
+    assert np.all(np.diff(y) >= 0)
+    # relative error within half a unit in the last place (normal range)
+    rel = np.abs(y - x) / np.abs(x)
+    assert rel.max() <= 2.0 ** -(mb + 1) * (1 + 1e-12)
+
+
+def _case(seed, BH, N, d):
+    rng = np.random.default_rng(seed)
+    q, k, v = (rng.standard_normal((BH, N, d)) for _ in range(3))
+    return q, k, v
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Bc", [1, 7, 64, 300])
+def test_emul_fp64_equals_definition(causal, Bc):
+    q, k, v = _case(6, 2, 150, 16)
+    scale = 0.25
+    want, _ = oracle.attn(q, k, v, causal, scale)
+    for algo in (0, 1):
+        got = oracle.emul(q, k, v, causal, scale, algo, Bc, 52, 11)
+        assert np.max(np.abs(got - want)) <= 1e-12, (algo, Bc)
+
+
+def test_emul_fp64_masked_and_fully_masked_rows():
+    q, k, v = _case(7, 2, 64, 8)
+    mask = np.where(np.random.default_rng(8).random((2, 64)) < 0.2, -np.inf, 0.0)
+    mask[0, :4] = -np.inf                      # causal rows 0..3 of head 0 see no key
+    want, _ = oracle.attn(q, k, v, True, 0.5, key_mask=mask)
+    for algo in (0, 1):
+        got = oracle.emul(q, k, v, True, 0.5, algo, 16, 52, 11, key_mask=mask)
+        assert np.max(np.abs(got - want)) <= 1e-12
+        assert np.all(got[0, :4] == 0.0)
+
+
+def test_emul_format_trend_of_fig3():
+    """FlashAttention vs baseline deviation falls as fraction bits grow."""
+    q, k, v = _case(9, 2, 512, 32)
+    scale = 1 / math.sqrt(32)
+    dev = {}
+    for fmt in ("bf16", "fp16", "fp32", "fp64"):
+        mb, eb = oracle.FORMATS[fmt]
+        base = oracle.emul(q, k, v, False, scale, 0, 64, mb, eb)
+        tiled = oracle.emul(q, k, v, False, scale, 1, 64, mb, eb)
+        dev[fmt] = np.max(np.abs(base - tiled))
+    assert dev["bf16"] > dev["fp16"] > dev["fp32"] > dev["fp64"]
+    assert dev["fp64"] <= 1e-13
+    assert dev["bf16"] > 1e-3
+
+
+def test_emul_row_subset_matches_full():
+    q, k, v = _case(10, 3, 40, 8)
+    full = oracle.emul(q, k, v, True, 0.3, 1, 8, 7, 8).reshape(-1, 8)
+    rows = np.array([0, 5, 39, 40, 119])
+    sub = oracle.emul(q, k, v, True, 0.3, 1, 8, 7, 8, rows=rows)
+    assert np.array_equal(sub, full[rows])
