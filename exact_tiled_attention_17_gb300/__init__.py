@@ -32,8 +32,8 @@ ATTN_ERR_DEVICE_TIMEOUT = -5
 
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_naive_workspace_size", "attn_naive_fwd", "attn_deviation_workspace_size",
-           "attn_deviation", "attn_deviation_noalloc", "attn_status", "attn_strerror", "attn_last_variant",
-           "attn_debug_wait_timeout")
+           "attn_deviation", "attn_deviation_noalloc", "attn_emul_fwd", "attn_emul_round", "attn_status",
+           "attn_strerror", "attn_last_variant", "attn_debug_wait_timeout")
 DEVIATION_NOALLOC_MAX_N = 1 << 20
 
 _DTYPE = {torch.float32: ATTN_F32, torch.bfloat16: ATTN_BF16, torch.float64: ATTN_F64}
@@ -68,6 +68,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_deviation.restype = i
     lib.attn_deviation_noalloc.argtypes = [vp, i, vp, i, ll, vp, ctypes.POINTER(DevT)]
     lib.attn_deviation_noalloc.restype = i
+    lib.attn_emul_fwd.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, f, vp, i, i, i, i, vp, ll, vp]
+    lib.attn_emul_fwd.restype = i
+    lib.attn_emul_round.argtypes = [vp, vp, ll, i, i, vp]
+    lib.attn_emul_round.restype = i
     lib.attn_status.argtypes = [vp]
     lib.attn_status.restype = i
     lib.attn_strerror.argtypes = [i]
@@ -213,6 +217,52 @@ def attn_deviation_noalloc(a, b, stream=None) -> dict:
     _check(rc, "attn_deviation_noalloc")
     return {"max_abs": res.max_abs, "w1": res.w1, "mean_abs": res.mean_abs, "std_abs": res.std_abs,
             "mean_signed": res.mean_signed, "n": res.n}
+
+
+# Number formats of the emulation (fraction bits, exponent bits).
+EMUL_FORMATS = {"bf16": (7, 8), "fp16": (10, 5), "tf32": (10, 8), "fp32": (23, 8), "fp64": (52, 11)}
+EMUL_BASELINE, EMUL_TILED = 0, 1
+
+
+def attn_emul_fwd(q, k, v, causal: bool, scale: float, algo: int, Bc: int, mbits: int, ebits: int,
+                  key_mask=None, rows=None, stream=None):
+    """Attention with every tensor op rounded to a number format (the
+    paper's numerical re-implementation; see include/attn.h).  q, k, v:
+    contiguous device tensors [B, H, N, d] (float32, bfloat16 or float64).
+    rows: None or a device int64 tensor of flat row ids.  Returns a float64
+    device tensor [B, H, N, d] (all rows) or [nrows, d]."""
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous device tensors")
+    B, H, N, d = _shape4(q)
+    if rows is None:
+        o = torch.empty((B, H, N, d), dtype=torch.float64, device=q.device)
+        nrows = 0
+    else:
+        if rows.dtype != torch.int64 or not rows.is_cuda or not rows.is_contiguous():
+            raise ValueError("rows must be a contiguous int64 device tensor")
+        nrows = rows.numel()
+        o = torch.empty((nrows, d), dtype=torch.float64, device=q.device)
+    m = None
+    if key_mask is not None:
+        m = key_mask
+        if m.dtype != torch.float32 or not m.is_contiguous() or m.numel() != B * H * N or not m.is_cuda:
+            raise ValueError("key_mask must be a contiguous float32 device tensor with B*H*N elements")
+    rc = lib.attn_emul_fwd(_ptr(q), _ptr(k), _ptr(v), _DTYPE[q.dtype], _ptr(o), B, H, N, d, int(bool(causal)),
+                           float(scale), _ptr(m), int(algo), int(Bc), int(mbits), int(ebits), _ptr(rows), nrows,
+                           ctypes.c_void_p(_stream(stream)))
+    _check(rc, "attn_emul_fwd")
+    return o
+
+
+def attn_emul_round(x, mbits: int, ebits: int, stream=None):
+    """fl(x) for a contiguous float64 device tensor (new tensor)."""
+    if x.dtype != torch.float64 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float64 device tensor")
+    y = torch.empty_like(x)
+    rc = lib.attn_emul_round(_ptr(x), _ptr(y), x.numel(), int(mbits), int(ebits), ctypes.c_void_p(_stream(stream)))
+    _check(rc, "attn_emul_round")
+    return y
 
 
 def attn_status(stream=None) -> int:

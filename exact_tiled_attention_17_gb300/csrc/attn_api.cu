@@ -198,6 +198,35 @@ int attn_deviation_noalloc(const void *a, int ta, const void *b, int tb, long lo
     return kOk;
 }
 
+int attn_emul_fwd(const void *Q, const void *K, const void *V, int dtype, double *O, int B, int H, int N, int d,
+                  int causal, float scale, const float *key_mask, int algo, int Bc, int mbits, int ebits,
+                  const long long *rows, long long nrows, void *stream) {
+    if (!Q || !K || !V || !O) return kErrArg;
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return kErrArg;
+    if (static_cast<long long>(B) * H * N >= (1LL << 31)) return kErrArg;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return kErrArg;
+    if (causal != 0 && causal != 1) return kErrArg;
+    if (dtype < ATTN_F32 || dtype > ATTN_F64) return kErrArg;
+    if (algo != ATTN_EMUL_BASELINE && algo != ATTN_EMUL_TILED) return kErrArg;
+    if (mbits < 1 || mbits > 52 || ebits < 2 || ebits > 11) return kErrArg;
+    if (rows && nrows < 0) return kErrArg;
+    if (algo == ATTN_EMUL_TILED && (Bc < 1 || Bc > ATTN_EMUL_MAX_BC)) return kErrArg;
+    if (d > 128) return kErrUnsupported;
+    if (algo == ATTN_EMUL_BASELINE && N > ATTN_EMUL_MAX_N_BASELINE) return kErrUnsupported;
+    if (key_mask && (reinterpret_cast<uintptr_t>(key_mask) & 3u)) return kErrArg;
+    if ((reinterpret_cast<uintptr_t>(O) & 7u) || (rows && (reinterpret_cast<uintptr_t>(rows) & 7u))) return kErrArg;
+    return launch_emul(Q, K, V, dtype, O, B, H, N, d, causal, scale, key_mask, algo, algo == ATTN_EMUL_TILED ? Bc : 1,
+                       mbits, ebits, rows, rows ? nrows : 0, static_cast<cudaStream_t>(stream));
+}
+
+int attn_emul_round(const double *x, double *y, long long n, int mbits, int ebits, void *stream) {
+    if (!x || !y || n < 0) return kErrArg;
+    if (mbits < 1 || mbits > 52 || ebits < 2 || ebits > 11) return kErrArg;
+    if ((reinterpret_cast<uintptr_t>(x) & 7u) || (reinterpret_cast<uintptr_t>(y) & 7u)) return kErrArg;
+    if (n == 0) return kOk;
+    return launch_fmt_round(x, y, n, mbits, ebits, static_cast<cudaStream_t>(stream));
+}
+
 int attn_status(void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(st) != cudaSuccess) return kErrCuda;
@@ -208,7 +237,7 @@ int attn_status(void *stream) {
     if (host != 0) {
         const int zero = 0;
         if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return kErrCuda;
-        return kErrDeviceTimeout;
+        return (host & ~kErrWordBadRow) ? kErrDeviceTimeout : kErrArg;
     }
     return kOk;
 }

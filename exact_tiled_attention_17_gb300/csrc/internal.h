@@ -23,6 +23,10 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
 
+// Error-word bit set by the emulation kernel for an out-of-range row id
+// (timed-out waits use the low bits).
+constexpr int kErrWordBadRow = 1 << 24;
+
 // Device address of the library's error word on the current device (or null).
 int *device_error_word();
 
@@ -51,6 +55,13 @@ size_t deviation_result_offset(long long n);
 constexpr long long kDeviationNoAllocMaxN = 1LL << 20;
 int launch_deviation_noalloc(const void *a, int ta, const void *b, int tb, long long n, cudaStream_t stream,
                              double *host_result /* 5 doubles */);
+
+// Number-format emulation (emul.cu).  dtype: 0 f32, 1 bf16, 2 f64.
+size_t emul_smem_bytes(int algo, int N, int Bc);
+int launch_emul(const void *Q, const void *K, const void *V, int dtype, double *O, int B, int H, int N, int d,
+                int causal, float scale, const float *key_mask, int algo, int Bc, int mbits, int ebits,
+                const long long *rows, long long nrows, cudaStream_t stream);
+int launch_fmt_round(const double *x, double *y, long long n, int mbits, int ebits, cudaStream_t stream);
 
 // Bounded-wait self-test kernel (attn_api.cu).
 int launch_wait_timeout_probe(unsigned timeout_us, cudaStream_t stream);

@@ -156,10 +156,64 @@ int attn_deviation_noalloc(const void *a, int ta, const void *b, int tb, long lo
                            attn_dev_t *out);
 
 /*
+ * Number-format emulation — the instrument of "Is Flash Attention Stable?"
+ * §III (Fig. 2): a numerical re-implementation of FlashAttention and of the
+ * baseline that can run in any number format and whose internals can be
+ * changed, used for the format sweep of §IV-A (Fig. 3) and the block-size
+ * perturbations of §IV-B (Fig. 6).  The pages give no code for it; the
+ * reading implemented here:
+ *
+ *  - A format has `mbits` fraction bits (1..52) and `ebits` exponent bits
+ *    (2..11), IEEE style: subnormals, round to nearest with ties to even,
+ *    overflow to infinity.  bf16 = (7, 8), fp16 = (10, 5), tf32 = (10, 8),
+ *    fp32 = (23, 8), fp64 = (52, 11).  fl(x) is x rounded to the format.
+ *  - Every tensor operation produces its result in the format: elementwise
+ *    operations are evaluated in binary64 and rounded once; reductions (row
+ *    sum, row maximum) and matrix products accumulate in binary64 and round
+ *    their result once.  Q, K and V are rounded to the format first.
+ *  - scores s_j = fl(scale * (q . k_j)), then fl(s_j + mask_j) with a key
+ *    mask (a -inf mask entry, or a causal future key, gives -inf).
+ *  - ATTN_EMUL_BASELINE: P = fl(softmax(s)) as one operation, O = fl(P V).
+ *  - ATTN_EMUL_TILED: the online merge over key blocks of width Bc, in
+ *    order: M = max(m, max_j s_j), M' = (M == -inf ? 0 : M),
+ *    a = fl(exp(fl(m - M'))) (0 while m is -inf), p_j = fl(exp(fl(s_j - M'))),
+ *    l = fl(fl(a*l) + fl(sum_j p_j)), o = fl(fl(a*o) + fl(sum_j p_j v_j));
+ *    finally O = fl(o / l), or 0 for a row with no allowed key.  Only the key
+ *    block width Bc changes a row's arithmetic; the query block height only
+ *    groups rows.
+ *
+ * attn_emul_fwd — Q, K, V: device, [B][H][N][d] of `dtype` (ATTN_F32,
+ * ATTN_BF16 or ATTN_F64), naturally aligned; key_mask as for attn_fwd.
+ * rows: device array of `nrows` flat row ids (bh * N + i), 8-byte aligned,
+ * or NULL for every row (nrows ignored).  O: device float64 [nrows][d]
+ * (or [B*H*N][d]), 8-byte aligned, row r for rows[r].  1 <= d <= 128;
+ * ATTN_EMUL_BASELINE needs N <= ATTN_EMUL_MAX_N_BASELINE (else
+ * ATTN_ERR_UNSUPPORTED); ATTN_EMUL_TILED needs 1 <= Bc <= ATTN_EMUL_MAX_BC.
+ * A row id out of range is skipped (its output row is left as it was) and
+ * the next attn_status() returns ATTN_ERR_ARG.  Binary64 arithmetic on the
+ * CUDA cores: a measurement tool, not a fast path.  Asynchronous.
+ */
+#define ATTN_EMUL_BASELINE 0
+#define ATTN_EMUL_TILED 1
+#define ATTN_EMUL_MAX_N_BASELINE 16384
+#define ATTN_EMUL_MAX_BC 4096
+int attn_emul_fwd(const void *Q, const void *K, const void *V, int dtype, double *O,
+                  int B, int H, int N, int d, int causal, float scale, const float *key_mask,
+                  int algo, int Bc, int mbits, int ebits, const long long *rows, long long nrows,
+                  void *stream);
+
+/*
+ * attn_emul_round — y[i] = fl(x[i]) for n float64 values in device memory
+ * (8-byte aligned; y may equal x), in the format (mbits, ebits) described
+ * above.  Asynchronous.
+ */
+int attn_emul_round(const double *x, double *y, long long n, int mbits, int ebits, void *stream);
+
+/*
  * attn_status — waits for `stream`, then returns ATTN_ERR_DEVICE_TIMEOUT if a
- * kernel of this library recorded a timed-out wait since the last call
- * (and clears the record), ATTN_ERR_CUDA if the stream reports a CUDA error,
- * else ATTN_OK.
+ * kernel of this library recorded a timed-out wait since the last call,
+ * ATTN_ERR_ARG if attn_emul_fwd met an out-of-range row id, and clears the
+ * record; ATTN_ERR_CUDA if the stream reports a CUDA error, else ATTN_OK.
  */
 int attn_status(void *stream);
 
