@@ -32,7 +32,8 @@ ATTN_ERR_DEVICE_TIMEOUT = -5
 
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_naive_workspace_size", "attn_naive_fwd", "attn_deviation_workspace_size",
-           "attn_deviation", "attn_deviation_noalloc", "attn_emul_fwd", "attn_emul_round", "attn_status",
+           "attn_deviation", "attn_deviation_noalloc", "attn_decode_workspace_size", "attn_decode_fwd",
+           "attn_emul_fwd", "attn_emul_round", "attn_status",
            "attn_strerror", "attn_last_variant", "attn_debug_wait_timeout")
 DEVIATION_NOALLOC_MAX_N = 1 << 20
 
@@ -68,6 +69,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_deviation.restype = i
     lib.attn_deviation_noalloc.argtypes = [vp, i, vp, i, ll, vp, ctypes.POINTER(DevT)]
     lib.attn_deviation_noalloc.restype = i
+    lib.attn_decode_workspace_size.argtypes = [i, i, i, i]
+    lib.attn_decode_workspace_size.restype = sz
+    lib.attn_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, sz, vp]
+    lib.attn_decode_fwd.restype = i
     lib.attn_emul_fwd.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, f, vp, i, i, i, i, vp, ll, vp]
     lib.attn_emul_fwd.restype = i
     lib.attn_emul_round.argtypes = [vp, vp, ll, i, i, vp]
@@ -217,6 +222,48 @@ def attn_deviation_noalloc(a, b, stream=None) -> dict:
     _check(rc, "attn_deviation_noalloc")
     return {"max_abs": res.max_abs, "w1": res.w1, "mean_abs": res.mean_abs, "std_abs": res.std_abs,
             "mean_signed": res.mean_signed, "n": res.n}
+
+
+DECODE_MAX_NQ = 8
+
+
+def attn_decode_workspace_size(B: int, H: int, Nq: int, d: int) -> int:
+    return int(lib.attn_decode_workspace_size(B, H, Nq, d))
+
+
+def attn_decode_fwd(q, k, v, causal: bool = False, scale: float | None = None, key_mask=None, out=None, lse=None,
+                    workspace=None, stream=None, want_lse: bool = True):
+    """Decode with a key/value cache.  q: [B, H, Nq, d]; k, v: [B, H, Nk, d]
+    contiguous device tensors of one dtype (bfloat16 or float32).  Causal:
+    query row i is the token at position Nk - Nq + i.  Returns (o, lse)."""
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous device tensors")
+    if k.shape != v.shape or q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("k and v must share a shape, and q, k, v a dtype")
+    B, H, Nq, d = _shape4(q)
+    Bk, Hk, Nk, dk = _shape4(k)
+    if (Bk, Hk, dk) != (B, H, d):
+        raise ValueError("q and k/v disagree on B, H or d")
+    if q.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = out if out is not None else torch.empty_like(q)
+    l = lse if lse is not None else (torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+                                     if want_lse else None)
+    need = attn_decode_workspace_size(B, H, Nq, d)
+    ws = workspace if workspace is not None else torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    m = None
+    if key_mask is not None:
+        m = key_mask
+        if m.dtype != torch.float32 or not m.is_contiguous() or m.numel() != B * H * Nk or not m.is_cuda:
+            raise ValueError("key_mask must be a contiguous float32 device tensor with B*H*Nk elements")
+    rc = lib.attn_decode_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, Nq, Nk, d, int(bool(causal)),
+                             float(scale), _DTYPE[q.dtype], _ptr(m), _ptr(ws), ws.numel(),
+                             ctypes.c_void_p(_stream(stream)))
+    _check(rc, "attn_decode_fwd")
+    return o, l
 
 
 # Number formats of the emulation (fraction bits, exponent bits).

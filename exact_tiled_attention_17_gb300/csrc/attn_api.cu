@@ -198,6 +198,32 @@ int attn_deviation_noalloc(const void *a, int ta, const void *b, int tb, long lo
     return kOk;
 }
 
+size_t attn_decode_workspace_size(int B, int H, int Nq, int d) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || d <= 0) return 0;
+    if (static_cast<long long>(B) * H * Nq >= (1LL << 31)) return 0;
+    return decode_workspace_bytes(B * H, Nq, d);
+}
+
+int attn_decode_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int Nq, int Nk,
+                    int d, int causal, float scale, int dtype, const float *key_mask, void *workspace,
+                    size_t ws_bytes, void *stream) {
+    if (!Q || !K || !V || !O) return kErrArg;
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return kErrArg;
+    if (static_cast<long long>(B) * H * Nk >= (1LL << 31) || static_cast<long long>(Nk) * d >= (1LL << 31))
+        return kErrArg;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return kErrArg;
+    if (causal != 0 && causal != 1) return kErrArg;
+    if (causal && Nq > Nk) return kErrArg;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return dtype == ATTN_F64 ? kErrUnsupported : kErrArg;
+    if (Nq > ATTN_DECODE_MAX_NQ || d > 128 || d % 32 != 0) return kErrUnsupported;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return kErrArg;
+    if (key_mask && (reinterpret_cast<uintptr_t>(key_mask) & 3u)) return kErrArg;
+    if (!workspace || ws_bytes < attn_decode_workspace_size(B, H, Nq, d) || !aligned16(workspace))
+        return kErrWorkspace;
+    return launch_decode(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, dtype == ATTN_BF16 ? 1 : 0, key_mask,
+                         workspace, static_cast<cudaStream_t>(stream));
+}
+
 int attn_emul_fwd(const void *Q, const void *K, const void *V, int dtype, double *O, int B, int H, int N, int d,
                   int causal, float scale, const float *key_mask, int algo, int Bc, int mbits, int ebits,
                   const long long *rows, long long nrows, void *stream) {

@@ -63,6 +63,13 @@ int launch_emul(const void *Q, const void *K, const void *V, int dtype, double *
                 const long long *rows, long long nrows, cudaStream_t stream);
 int launch_fmt_round(const double *x, double *y, long long n, int mbits, int ebits, cudaStream_t stream);
 
+// Decode with a key/value cache (decode.cu).
+constexpr int kDecodeMaxSplits = 128;
+size_t decode_workspace_bytes(int BH, int Nq, int d);
+int launch_decode(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int Nq, int Nk,
+                  int d, int causal, float scale, int bf16, const float *key_mask, void *workspace,
+                  cudaStream_t stream);
+
 // Bounded-wait self-test kernel (attn_api.cu).
 int launch_wait_timeout_probe(unsigned timeout_us, cudaStream_t stream);
 

@@ -216,6 +216,17 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src,
         "r"(src), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
+// Untiled bulk copy global -> shared (both addresses 16-byte aligned, size a
+// multiple of 16), completing `bytes` on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void tma_store_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");

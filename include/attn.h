@@ -156,6 +156,31 @@ int attn_deviation_noalloc(const void *a, int ta, const void *b, int tb, long lo
                            attn_dev_t *out);
 
 /*
+ * attn_decode_fwd — decode with a key/value cache: attention of Nq new query
+ * rows against Nk cached keys and values, the same exact attention as
+ * attn_fwd ("Is Flash Attention Stable?" §II-A), evaluated by splitting the
+ * keys into chunks and merging the chunks' partial results with the
+ * yadro-code.ru tutorial's rule for joining two blocks (common maximum,
+ * weights exp(m - M)).
+ *
+ * Q: [B][H][Nq][d]; K, V: [B][H][Nk][d] (the cache); O: [B][H][Nq][d], all of
+ * `dtype` (ATTN_BF16 or ATTN_F32), 16-byte aligned.  LSE: [B][H][Nq] float32
+ * natural log, or NULL.  key_mask: NULL or [B][H][Nk] additive (finite or
+ * -inf).  causal: query row i is the token at position Nk - Nq + i and sees
+ * keys j <= Nk - Nq + i (needs Nq <= Nk); otherwise every row sees every
+ * key.  A row with no allowed key gives O = 0, LSE = -inf.
+ * 1 <= Nq <= ATTN_DECODE_MAX_NQ and d in {32, 64, 96, 128}, else
+ * ATTN_ERR_UNSUPPORTED.  workspace: device memory of at least
+ * attn_decode_workspace_size(B, H, Nq, d) bytes, 16-byte aligned, for the
+ * chunks' partial results.  HBM-bound: runs on the CUDA cores.  Asynchronous.
+ */
+#define ATTN_DECODE_MAX_NQ 8
+size_t attn_decode_workspace_size(int B, int H, int Nq, int d);
+int attn_decode_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                    int B, int H, int Nq, int Nk, int d, int causal, float scale, int dtype,
+                    const float *key_mask, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Number-format emulation — the instrument of "Is Flash Attention Stable?"
  * §III (Fig. 2): a numerical re-implementation of FlashAttention and of the
  * baseline that can run in any number format and whose internals can be
