@@ -19,7 +19,7 @@
 //     consumers' states are merged in shared memory; one partial per (split,
 //     b, h, row) goes to the workspace (or straight to O and LSE when there is
 //     one split).
-//   merge kernel, one CTA per (b, h, row), d threads.
+//   merge kernel, one CTA per (b, h, row), 128 threads.
 // Causal decoding: query row i is the token at position Nk - Nq + i and sees
 // keys j <= Nk - Nq + i.
 #include <cuda_bf16.h>
@@ -314,27 +314,34 @@ __global__ void __launch_bounds__(32 * (kDecWarps + 1)) decode_partial_kernel(co
     }
 }
 
-// one CTA per (b, h, row): merge the splits' partials
-__global__ void decode_merge_kernel(const DecParams p) {
+// one CTA per (b, h, row): merge the splits' partials.  The splits' (m, l)
+// are read in parallel and their weights 2^(m_s - M) kept in shared memory, so
+// the per-column sums over the splits issue all their loads at once.
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecParams p) {
+    __shared__ float wsh[kDecodeMaxSplits];
+    __shared__ float red[4];
     const long long row = blockIdx.x;   // bh * Nq + i
     const long long nrow = static_cast<long long>(p.BH) * p.Nq;
-    float M = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, p.pm[s * nrow + row]);
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const float ms = t < p.splits ? p.pm[t * nrow + row] : -INFINITY;
+    float M = warp_max(ms);
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
     const float mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f;
-    for (int s = 0; s < p.splits; ++s) {
-        const float ms = p.pm[s * nrow + row];
-        L += (ms == -INFINITY) ? 0.f : ex2(ms - mu) * p.pl[s * nrow + row];
-    }
-    for (int c = threadIdx.x; c < p.d; c += blockDim.x) {
+    const float w = (ms == -INFINITY) ? 0.f : ex2(ms - mu);
+    if (t < p.splits) wsh[t] = w;
+    float L = warp_sum(t < p.splits ? w * p.pl[t * nrow + row] : 0.f);
+    if (lane == 0) red[warp] = L;
+    __syncthreads();
+    L = red[0] + red[1] + red[2] + red[3];
+    for (int c = t; c < p.d; c += blockDim.x) {
         float acc = 0.f;
-        for (int s = 0; s < p.splits; ++s) {
-            const float ms = p.pm[s * nrow + row];
-            if (ms != -INFINITY) acc += ex2(ms - mu) * p.po[(s * nrow + row) * p.d + c];
-        }
+        for (int s = 0; s < p.splits; ++s) acc += wsh[s] * p.po[(s * nrow + row) * p.d + c];
         store_out(p.O, p.bf16, row * p.d + c, L > 0.f ? acc / L : 0.f);
     }
-    if (threadIdx.x == 0 && p.LSE) p.LSE[row] = L > 0.f ? (M + log2f(L)) * kLn2D : -INFINITY;
+    if (t == 0 && p.LSE) p.LSE[row] = L > 0.f ? (M + log2f(L)) * kLn2D : -INFINITY;
 }
 
 template <int NQ, int E>
@@ -432,7 +439,7 @@ int launch_decode(const void *Q, const void *K, const void *V, void *O, float *L
     if (rc != kOk) return rc;
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     if (p.splits > 1) {
-        decode_merge_kernel<<<static_cast<unsigned>(p.BH * Nq), d, 0, stream>>>(p);
+        decode_merge_kernel<<<static_cast<unsigned>(p.BH * Nq), 128, 0, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     }
     return kOk;
