@@ -28,6 +28,10 @@ emul(q, k, v, causal, scale, algo, Bc, mbits, ebits, key_mask=None, rows=None)
     The paper's numerical re-implementation (§III, §IV-A Fig. 3): baseline
     (algo 0) or tiled (algo 1, key blocks of width Bc) attention with every
     tensor operation's result rounded to that format (``oracle_emul.c``).
+attn_bwd(q, k, v, do, causal, scale, key_mask=None, heads=None)
+    dL/dQ, dL/dK, dL/dV of the same definition for an upstream gradient dO,
+    by the chain rule through the softmax, row by row in binary64
+    (``oracle_bwd.c``).
 """
 from __future__ import annotations
 
@@ -41,6 +45,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle_attn.c")
 _SRC_EMUL = os.path.join(_HERE, "oracle_emul.c")
+_SRC_BWD = os.path.join(_HERE, "oracle_bwd.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -49,13 +54,13 @@ ORACLE_NO_RESCALE = 1
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle_attn.c and oracle_emul.c into liboracle.so next to them (gcc, -O2, no fast-math)."""
-    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_EMUL))
+    """Compile the oracle's C files into liboracle.so next to them (gcc, -O2, no fast-math)."""
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_EMUL), os.path.getmtime(_SRC_BWD))
     if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= newest:
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fno-fast-math", "-fPIC", "-shared",
-           "-o", tmp, _SRC, _SRC_EMUL, "-lm", "-lpthread"]
+           "-o", tmp, _SRC, _SRC_EMUL, _SRC_BWD, "-lm", "-lpthread"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -85,6 +90,10 @@ def _load():
                                              ctypes.c_int, ctypes.c_int, lp, ctypes.c_longlong, dp,
                                              ctypes.c_int]
             lib.oracle_emul_rows.restype = ctypes.c_int
+            lib.oracle_attn_bwd_f64.argtypes = [dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_double, lp, ctypes.c_longlong,
+                                                dp, dp, dp, ctypes.c_int, ctypes.c_int]
+            lib.oracle_attn_bwd_f64.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -230,3 +239,44 @@ def emul(q, k, v, causal: bool, scale: float, algo: int, Bc: int, mbits: int, eb
     if rc != 0:
         raise RuntimeError("oracle_emul_rows failed")
     return O.reshape(*lead, N, d) if R is None else O
+
+
+ORACLE_BWD_PLANT_NO_CENTER = 1   # drop the softmax Jacobian's rank-one term (planted mistake)
+ORACLE_BWD_PLANT_NO_SCALE = 2    # leave `scale` out of dQ and dK (planted mistake)
+
+
+def attn_bwd(q, k, v, do, causal: bool, scale: float, key_mask=None, heads=None, plant: int = 0,
+             nthreads: int | None = None):
+    """Binary64 gradients of attention for the upstream gradient ``do``.
+
+    q, k, v, do: [..., N, d] (leading dims flattened to BH); key_mask: None
+    or [..., N] additive.  heads: None for every head, else integer head ids
+    bh.  Returns (dQ, dK, dV), each [..., N, d] for all heads or
+    [nheads, N, d] for a subset.  ``plant`` is for the oracle's own tests.
+    """
+    lib = _load()
+    Q, K, V, dO = _f64(q), _f64(k), _f64(v), _f64(do)
+    if not (Q.shape == K.shape == V.shape == dO.shape) or Q.ndim < 2:
+        raise ValueError("q, k, v, do must share one shape [..., N, d]")
+    lead = Q.shape[:-2]
+    N, d = Q.shape[-2], Q.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    M = None
+    if key_mask is not None:
+        M = _f64(key_mask)
+        if M.size != BH * N:
+            raise ValueError("key_mask must have BH*N elements")
+    Hs = None if heads is None else np.ascontiguousarray(np.asarray(heads, dtype=np.int64))
+    nh = BH if Hs is None else Hs.size
+    dQ = np.zeros((nh, N, d), dtype=np.float64)
+    dK = np.zeros((nh, N, d), dtype=np.float64)
+    dV = np.zeros((nh, N, d), dtype=np.float64)
+    rc = lib.oracle_attn_bwd_f64(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(M) if M is not None else None,
+                                 BH, N, d, 1 if causal else 0, float(scale),
+                                 _ptr(Hs, ctypes.c_longlong) if Hs is not None else None, nh,
+                                 _ptr(dQ), _ptr(dK), _ptr(dV), int(plant), nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_attn_bwd_f64 failed")
+    if heads is None:
+        return dQ.reshape(*lead, N, d), dK.reshape(*lead, N, d), dV.reshape(*lead, N, d)
+    return dQ, dK, dV
