@@ -33,7 +33,7 @@ ATTN_ERR_DEVICE_TIMEOUT = -5
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_naive_workspace_size", "attn_naive_fwd", "attn_deviation_workspace_size",
            "attn_deviation", "attn_deviation_noalloc", "attn_decode_workspace_size", "attn_decode_fwd",
-           "attn_emul_fwd", "attn_emul_round", "attn_status",
+           "attn_bwd_workspace_size", "attn_bwd", "attn_emul_fwd", "attn_emul_round", "attn_status",
            "attn_strerror", "attn_last_variant", "attn_debug_wait_timeout")
 DEVIATION_NOALLOC_MAX_N = 1 << 20
 
@@ -73,6 +73,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_decode_workspace_size.restype = sz
     lib.attn_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, sz, vp]
     lib.attn_decode_fwd.restype = i
+    lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.attn_bwd_workspace_size.restype = sz
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, sz, vp]
+    lib.attn_bwd.restype = i
     lib.attn_emul_fwd.argtypes = [vp, vp, vp, i, vp, i, i, i, i, i, f, vp, i, i, i, i, vp, ll, vp]
     lib.attn_emul_fwd.restype = i
     lib.attn_emul_round.argtypes = [vp, vp, ll, i, i, vp]
@@ -264,6 +268,45 @@ def attn_decode_fwd(q, k, v, causal: bool = False, scale: float | None = None, k
                              ctypes.c_void_p(_stream(stream)))
     _check(rc, "attn_decode_fwd")
     return o, l
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(lib.attn_bwd_workspace_size(B, H, N, d))
+
+
+def attn_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None, key_mask=None,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients of attention.  q, k, v, o, do: [B, H, N, d] contiguous
+    bfloat16 device tensors (o and lse from attn_fwd on the same inputs);
+    lse: [B, H, N] float32.  Returns (dq, dk, dv)."""
+    ts = (q, k, v, o, do)
+    for t in ts:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, o, do must be contiguous device tensors")
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("q, k, v, o, do must share one shape and dtype")
+    B, H, N, d = _shape4(q)
+    if q.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or lse.numel() != B * H * N):
+        raise ValueError("lse must be a contiguous float32 device tensor with B*H*N elements")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(q)
+    dv = dv if dv is not None else torch.empty_like(q)
+    need = attn_bwd_workspace_size(B, H, N, d)
+    ws = workspace if workspace is not None else torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    m = None
+    if key_mask is not None:
+        m = key_mask
+        if m.dtype != torch.float32 or not m.is_contiguous() or m.numel() != B * H * N or not m.is_cuda:
+            raise ValueError("key_mask must be a contiguous float32 device tensor with B*H*N elements")
+    rc = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                      B, H, N, d, int(bool(causal)), float(scale), _DTYPE[q.dtype], _ptr(m), _ptr(ws), ws.numel(),
+                      ctypes.c_void_p(_stream(stream)))
+    _check(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 # Number formats of the emulation (fraction bits, exponent bits).

@@ -224,6 +224,38 @@ int attn_decode_fwd(const void *Q, const void *K, const void *V, void *O, float 
                          workspace, static_cast<cudaStream_t>(stream));
 }
 
+size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+    if (static_cast<long long>(B) * H * N >= (1LL << 31)) return 0;
+    return bwd_workspace_bytes(B * H, N, d);
+}
+
+int attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE, void *dQ,
+             void *dK, void *dV, int B, int H, int N, int d, int causal, float scale, int dtype,
+             const float *key_mask, void *workspace, size_t ws_bytes, void *stream) {
+    int rc = check_common(Q, K, V, const_cast<void *>(O), B, H, N, d, scale, key_mask);
+    if (rc != kOk) return rc;
+    if (!dO || !LSE || !dQ || !dK || !dV) return kErrArg;
+    if (!aligned16(dO) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV)) return kErrArg;
+    if (reinterpret_cast<uintptr_t>(LSE) & 3u) return kErrArg;
+    if (causal != 0 && causal != 1) return kErrArg;
+    if (dtype != ATTN_BF16) return (dtype == ATTN_F32 || dtype == ATTN_F64) ? kErrUnsupported : kErrArg;
+    if (d != 64 && d != 128) return kErrUnsupported;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return kErrCuda;
+    if (major != 10 || minor != 3) return kErrUnsupported;  // built for sm_103a only
+    if (!workspace || ws_bytes < attn_bwd_workspace_size(B, H, N, d) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return kErrWorkspace;
+    rc = launch_bwd_tc_bf16(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, causal, scale, key_mask, workspace,
+                            static_cast<cudaStream_t>(stream));
+    if (rc == kOk) t_last_variant = d == 64 ? "bwd_tc_bf16_d64_br64_bc128" : "bwd_tc_bf16_d128_br64_bc128";
+    return rc;
+}
+
 int attn_emul_fwd(const void *Q, const void *K, const void *V, int dtype, double *O, int B, int H, int N, int d,
                   int causal, float scale, const float *key_mask, int algo, int Bc, int mbits, int ebits,
                   const long long *rows, long long nrows, void *stream) {

@@ -70,6 +70,12 @@ int launch_decode(const void *Q, const void *K, const void *V, void *O, float *L
                   int d, int causal, float scale, int bf16, const float *key_mask, void *workspace,
                   cudaStream_t stream);
 
+// Backward on tcgen05 (bwd_tc.cu).
+size_t bwd_workspace_bytes(int BH, int N, int d);
+int launch_bwd_tc_bf16(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+                       void *dQ, void *dK, void *dV, int B, int H, int N, int d, int causal, float scale,
+                       const float *key_mask, void *workspace, cudaStream_t stream);
+
 // Bounded-wait self-test kernel (attn_api.cu).
 int launch_wait_timeout_probe(unsigned timeout_us, cudaStream_t stream);
 

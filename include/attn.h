@@ -181,6 +181,33 @@ int attn_decode_fwd(const void *Q, const void *K, const void *V, void *O, float 
                     const float *key_mask, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * attn_bwd — gradients of exact attention: for O = softmax(Q K^T * scale +
+ * mask) V ("Is Flash Attention Stable?" §II-A) and an upstream gradient dO,
+ * dQ, dK and dV.  As the yadro-code.ru FlashAttention tutorial describes for
+ * the method's backward pass, intermediate values are recomputed rather than
+ * stored: the attention weights are formed again, tile by tile, from Q, K and
+ * the forward's per-row LSE, P = exp(s - LSE); nothing of size N x N is kept.
+ *
+ * Q, K, V, O, dO: [B][H][N][d] bfloat16 (O and LSE as attn_fwd wrote them for
+ * these Q, K, V, causal, scale and mask); LSE: [B][H][N] float32 natural log
+ * (-inf for a row with no allowed key: its gradients are 0).  dQ, dK, dV:
+ * [B][H][N][d] bfloat16, written.  All tensor pointers 16-byte aligned,
+ * caller-owned device memory.  key_mask: NULL or [B][H][N] additive (finite
+ * or -inf), a constant (no gradient is formed for it).  causal as attn_fwd.
+ * dtype must be ATTN_BF16 and d 64 or 128, else ATTN_ERR_UNSUPPORTED.
+ * workspace: at least attn_bwd_workspace_size(B, H, N, d) bytes of device
+ * memory, 256-byte aligned (the rows' LSE and D = rowsum(dO * O) vectors and
+ * a float32 dQ accumulator), else ATTN_ERR_WORKSPACE.  Asynchronous: three
+ * launches on `stream`; errors in the arguments are returned before any
+ * launch.  dQ is accumulated with floating-point atomics, so its last bits
+ * can differ from run to run; dK and dV are deterministic.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+int attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+             void *dQ, void *dK, void *dV, int B, int H, int N, int d, int causal, float scale, int dtype,
+             const float *key_mask, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Number-format emulation — the instrument of "Is Flash Attention Stable?"
  * §III (Fig. 2): a numerical re-implementation of FlashAttention and of the
  * baseline that can run in any number format and whose internals can be

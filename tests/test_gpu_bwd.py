@@ -1,0 +1,114 @@
+"""Gradients of attention on the GPU (attn_bwd) against the FP64 oracle.
+
+The forward runs on the GPU (attn_fwd) and hands O and the per-row LSE to the
+backward, as in training; the oracle (``oracle.attn_bwd``) differentiates the
+definition of attention directly from the same bf16 Q, K, V and dO, upcast
+exactly to binary64.
+
+Tolerance, derived from the arithmetic: the products of bf16 operands are
+exact and accumulate in float32; the rounding that matters is P, dS and the
+gradients themselves going to bf16 (relative 2^-9 each) and O (which enters
+through D = rowsum(dO * O)) being bf16.  Each gradient element is a sum of
+such rounded terms, so its error is a small multiple of 2^-9 times the
+largest magnitude of the tensor.  The test bound is 2e-2 (about 10 * 2^-9)
+times max(1, max |reference|) per tensor, the bf16 bound the forward uses, and
+a relative Frobenius error below 1e-2.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def eta():
+    import exact_tiled_attention_17_gb300 as m
+    return m
+
+
+def _run(eta, B, H, N, d, causal, seed, mask=None, qk_scale=1.0):
+    q, k, v = workloads.make_qkv(B, H, N, d, "bf16", seed, qk_scale)
+    do = workloads.make_grad_out(B, H, N, d, "bf16", seed)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    mc = mask.cuda() if mask is not None else None
+    o, lse = eta.attn_fwd(qc, kc, vc, causal, scale, key_mask=mc)
+    dq, dk, dv = eta.attn_bwd(qc, kc, vc, o, doc, lse, causal, scale, key_mask=mc)
+    assert eta.attn_status() == 0
+    return (q, k, v, do, scale), (dq, dk, dv)
+
+
+def _compare(got, want, label):
+    g = got.double().cpu().numpy()
+    assert not np.isnan(g).any(), label
+    err = np.abs(g - want)
+    ref = max(1.0, float(np.max(np.abs(want))))
+    assert err.max() <= 2e-2 * ref, (label, float(err.max()), ref)
+    nw = float(np.linalg.norm(want))
+    fro = float(np.linalg.norm(g - want)) / nw if nw > 1e-6 * math.sqrt(want.size) else 0.0
+    assert fro <= 1e-2, (label, fro)     # (a gradient that is 0 by the definition has no relative error)
+    print(f"{label}: max|err|/max(1,max|ref|) = {float(err.max()) / ref:.3e}, relative Frobenius = {fro:.3e}")
+    return float(err.max()) / ref, fro
+
+
+def _check(eta, B, H, N, d, causal, seed, mask=None, heads=None):
+    (q, k, v, do, scale), (dq, dk, dv) = _run(eta, B, H, N, d, causal, seed, mask)
+    wq, wk, wv = oracle.attn_bwd(q, k, v, do, causal, scale, key_mask=mask, heads=heads)
+    sel = (lambda t: t.reshape(B * H, N, d)[heads]) if heads is not None else (lambda t: t.reshape(wq.shape))
+    wq, wk, wv = (x.reshape(-1, N, d) for x in (wq, wk, wv))
+    out = {}
+    for name, got, want in (("dQ", dq, wq), ("dK", dk, wk), ("dV", dv, wv)):
+        g = sel(got.cpu()).reshape(-1, N, d)
+        out[name] = _compare(g, want, name)
+    return out, (dq, dk, dv)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 63, 200, 384])
+def test_bwd_bf16_matches_oracle(eta, d, causal, N):
+    _check(eta, 1, 3, N, d, causal, seed=N + d)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_key_mask_and_fully_masked_rows(eta, causal):
+    B, H, N, d = 1, 4, 300, 64
+    mask = workloads.make_key_mask(B, H, N, 0.1, seed=7)   # heads 0 mod 4: keys 0..3 masked
+    mask[0, 3, :] = -float("inf")                          # head 3: every key masked
+    _, (dq, dk, dv) = _check(eta, B, H, N, d, causal, seed=7, mask=mask)
+    # a row without any allowed key has O = 0, a constant: its gradients are 0
+    assert torch.all(dq[0, 3] == 0) and torch.all(dk[0, 3] == 0) and torch.all(dv[0, 3] == 0)
+    if causal:
+        assert torch.all(dq[0, 0, :4] == 0)
+
+
+def test_bwd_dk_dv_deterministic(eta):
+    a = _run(eta, 1, 2, 500, 128, True, seed=3)[1]
+    b = _run(eta, 1, 2, 500, 128, True, seed=3)[1]
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2
+
+
+def test_bwd_rejects_unsupported(eta):
+    q = torch.zeros((1, 1, 64, 64), dtype=torch.float32, device="cuda")
+    lse = torch.zeros((1, 1, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(eta.AttnError):
+        eta.attn_bwd(q, q, q, q, q, lse)                    # float32: bf16 only
+    qb = torch.zeros((1, 1, 64, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(eta.AttnError):
+        eta.attn_bwd(qb, qb, qb, qb, qb, lse)               # d = 96
+    q2 = torch.zeros((1, 1, 64, 64), dtype=torch.bfloat16, device="cuda")
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(eta.AttnError):
+        eta.attn_bwd(q2, q2, q2, q2, q2, lse, workspace=small)
+
+
+def test_bwd_full_size_sampled_heads(eta):
+    """The bench shape 2x16x4096x128 (non-causal), two heads checked whole."""
+    _check(eta, 2, 16, 4096, 128, False, seed=0, heads=[0, 31])

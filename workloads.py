@@ -90,6 +90,15 @@ def make_qkv(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int = 0,
     return q.to(t).contiguous(), k.to(t).contiguous(), v.to(t).contiguous()
 
 
+def make_grad_out(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int = 0):
+    """Upstream gradient dO for the backward pass: float32 N(0, 1) from its own
+    stream (seed + 3, so it does not disturb Q/K/V or the mask), rounded to
+    the storage dtype, [B][H][N][d] contiguous on the CPU."""
+    g = torch.Generator(device="cpu").manual_seed(seed + 3)
+    do = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
+    return do.to(TORCH_DTYPE[dtype]).contiguous()
+
+
 def make_key_mask(B: int, H: int, N: int, frac: float, seed: int = 0,
                   force_masked_heads_every: int = 4, force_masked_keys: int = 4):
     """Additive key-padding mask, float32 [B][H][N], entries 0 or -inf.
