@@ -17,22 +17,27 @@
 //          resident in shared memory, query tiles of BR = 64 rows streamed:
 //            warps 0..7  two warpgroups, each thread one key row (tensor
 //                        memory lane = key); warpgroup h owns query columns
-//                        32h .. 32h+31 of S^T and dP^T.  P^T and dS^T go back
-//                        to tensor memory as bf16, dS also to shared memory
-//                        (the A operand of dS K); then the M = 64 dQ partial
-//                        of the step is added into the f32 accumulator in
-//                        global memory (vector reductions).
+//                        32h .. 32h+31 of S^T and dP^T.  They load S^T and
+//                        dP^T and release them at once, form P and dS in
+//                        registers, and write P^T and dS^T (bf16) into their
+//                        own tensor-memory columns and dS^T into shared memory
+//                        (an operand of the dQ product).  Then the previous
+//                        step's dQ^T partial is added into the f32 accumulator
+//                        in global memory: lane = head-dim index, so each
+//                        warp-wide reduction covers one 128-byte line.
 //            warp 8      TMA producer: K_j, V_j once; Q_i, dO_i tiles and the
 //                        step's LSE / D slices into a ring of NS stages.
 //            warp 9      MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T (both
-//                        operands in shared memory); then dV += P^T dO_i and
-//                        dK += dS^T Q_i (A from tensor memory, B MN-major in
-//                        shared memory) and dQ_i = dS K_j (A MN-major in shared
-//                        memory, B the resident K tile read MN-major).
+//                        operands in shared memory), issued for step i+1 as
+//                        soon as the warps hold step i's; then dV += P^T dO_i
+//                        and dK += dS^T Q_i (A from tensor memory, B MN-major
+//                        in shared memory) and dQ_i^T = K_j^T dS_i^T (both
+//                        MN-major in shared memory, M = d).
 //          Epilogue: dV and scale * dK to bf16, staged over the K / V tiles,
 //          TMA-stored.
 //   finish dQ = bf16(scale * accumulator).
-// Tensor memory (512 columns): S^T | dP^T (64 each) | dV | dK | dQ partial (D each).
+// Tensor memory (512 columns for d = 128):
+//   S^T | dP^T (64 each) | P^T | dS^T (bf16, 32 each) | dV | dK (d each) | dQ^T (64).
 #include <cuda_bf16.h>
 #include <cstdio>
 
@@ -55,7 +60,7 @@ struct BwdShape {
     static constexpr int QT_BYTES = BR * D * 2;      // one Q or dO tile
     static constexpr int STAGE_BYTES = 2 * QT_BYTES; // Q_i | dO_i
     static constexpr int STAT_BYTES = 2 * BR * 4;    // LSE (log2) | D of the step's rows
-    static constexpr int DS_BYTES = BR * BC * 2;     // dS, MN-major A operand of dS K
+    static constexpr int DS_BYTES = BR * BC * 2;     // dS^T, MN-major B operand of K^T dS^T
     static constexpr int NS = 4;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = KV_BYTES;
@@ -63,14 +68,15 @@ struct BwdShape {
     static constexpr int OFF_DS = OFF_RING + NS * STAGE_BYTES;
     static constexpr int OFF_STAT = OFF_DS + DS_BYTES;
     static constexpr int OFF_BAR = OFF_STAT + NS * STAT_BYTES;
-    // barriers: kv_full, full[NS], empty[NS], s_full, ds_ready, dq_full, done
+    // barriers: kv_full, full[NS], empty[NS], s_full, s_free, ds_ready, b_done, done
     static constexpr int BAR_KV = 0;
     static constexpr int BAR_FULL = 1;
     static constexpr int BAR_EMPTY = BAR_FULL + NS;
-    static constexpr int BAR_SFULL = BAR_EMPTY + NS;
-    static constexpr int BAR_DSREADY = BAR_SFULL + 1;
-    static constexpr int BAR_DQFULL = BAR_DSREADY + 1;
-    static constexpr int BAR_DONE = BAR_DQFULL + 1;
+    static constexpr int BAR_SFULL = BAR_EMPTY + NS;    // S^T, dP^T of a step are in tensor memory
+    static constexpr int BAR_SFREE = BAR_SFULL + 1;     // ... and the warps hold them in registers
+    static constexpr int BAR_DSREADY = BAR_SFREE + 1;   // P^T, dS^T, dS^T (shared) of a step written
+    static constexpr int BAR_BDONE = BAR_DSREADY + 1;   // the step's dV, dK, dQ^T products are done
+    static constexpr int BAR_DONE = BAR_BDONE + 1;
     static constexpr int NBARS = BAR_DONE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     // + alignment slack; at least 117 KB so that no second CTA is resident
@@ -78,11 +84,13 @@ struct BwdShape {
     static constexpr int SMEM_MIN = OFF_MISC + 16 + 1024;
     static constexpr int SMEM_BYTES = SMEM_MIN < 117 * 1024 ? 117 * 1024 : SMEM_MIN;
     // tensor memory columns
-    static constexpr int C_S = 0;              // S^T (f32), then P^T (bf16 pairs)
-    static constexpr int C_DP = BR;            // dP^T (f32), then dS^T (bf16 pairs)
-    static constexpr int C_DV = 2 * BR;
-    static constexpr int C_DK = 2 * BR + D;
-    static constexpr int C_DQ = 2 * BR + 2 * D;   // M = 64 accumulator
+    static constexpr int C_S = 0;              // S^T (f32)
+    static constexpr int C_DP = BR;            // dP^T (f32)
+    static constexpr int C_P = 2 * BR;         // P^T (bf16 pairs)
+    static constexpr int C_DS = 2 * BR + BR / 2;   // dS^T (bf16 pairs)
+    static constexpr int C_DV = 3 * BR;
+    static constexpr int C_DK = 3 * BR + D;
+    static constexpr int C_DQ = 3 * BR + 2 * D;    // dQ^T: M = d rows (lanes), BR columns
     static constexpr int TMEM_COLS = 512;
     static constexpr int COMPUTE_WARPS = 8;
     static constexpr int WARP_TMA = COMPUTE_WARPS;
@@ -90,7 +98,7 @@ struct BwdShape {
     static constexpr int THREADS = 32 * (COMPUTE_WARPS + 2);
 
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(C_DQ + D <= TMEM_COLS, "tensor memory budget");
+    static_assert(C_DQ + BR <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(BR == 64 && COMPUTE_WARPS == 8, "two warpgroups of 32 query columns each");
 };
@@ -157,8 +165,9 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
             mbar_init(bar(S::BAR_EMPTY + s), 1);
         }
         mbar_init(bar(S::BAR_SFULL), 1);
+        mbar_init(bar(S::BAR_SFREE), 32 * S::COMPUTE_WARPS);
         mbar_init(bar(S::BAR_DSREADY), 32 * S::COMPUTE_WARPS);
-        mbar_init(bar(S::BAR_DQFULL), 1);
+        mbar_init(bar(S::BAR_BDONE), 1);
         mbar_init(bar(S::BAR_DONE), 1);
         *abort_flag = 0u;
         fence_mbar_init();
@@ -231,21 +240,20 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
             // --------------------------------------------------------------
             constexpr uint32_t idesc_s = idesc_bf16_f32(128, BR, false, false);  // S^T, dP^T: K-major A and B
             constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, false, true);    // dV, dK: A in TMEM, B MN-major
-            constexpr uint32_t idesc_q = idesc_bf16_f32(BR, D, true, true);      // dQ: A, B MN-major
+            constexpr uint32_t idesc_q = idesc_bf16_f32(D, BR, true, true);      // dQ^T: A, B MN-major
             bool ok = wwait(bar(S::BAR_KV), 0, 10);
             const uint64_t kdesc = sdesc_sw128(sK, 16, 1024);              // K as K-major A
             const uint64_t vdesc = sdesc_sw128(sV, 16, 1024);              // V as K-major A
-            const uint64_t kdesc_mn = sdesc_sw128(sK, BC * 128, 1024);     // K as MN-major B (keys = K dim)
-            const uint64_t dsdesc = sdesc_sw128(sDS, 16, 1024);             // dS as MN-major A (one 64-wide atom in M)
-            for (int t = 0; ok && t < nit; ++t) {
+            const uint64_t ktdesc = sdesc_sw128(sK, BC * 128, 1024);       // K^T as MN-major A (keys = K dim)
+            const uint64_t dsdesc = sdesc_sw128(sDS, 16, 1024);            // dS^T as MN-major B (one 64-wide atom)
+            // S^T = K Q_t^T and dP^T = V dO_t^T of step t (stage t % NS)
+            auto issue_a = [&](int t) -> bool {
                 const int slot = t % S::NS;
-                if (!wwait(bar(S::BAR_FULL + slot), (t / S::NS) & 1, 11)) break;
+                if (!wwait(bar(S::BAR_FULL + slot), (t / S::NS) & 1, 11)) return false;
                 tc_fence_after();
                 const uint32_t st = sRing + slot * S::STAGE_BYTES;
-                const uint64_t qdesc = sdesc_sw128(st, 16, 1024);                       // Q_i as K-major B
-                const uint64_t dodesc = sdesc_sw128(st + S::QT_BYTES, 16, 1024);        // dO_i as K-major B
-                const uint64_t qdesc_mn = sdesc_sw128(st, BR * 128, 1024);              // Q_i as MN-major B
-                const uint64_t dodesc_mn = sdesc_sw128(st + S::QT_BYTES, BR * 128, 1024);
+                const uint64_t qdesc = sdesc_sw128(st, 16, 1024);                  // Q_t as K-major B
+                const uint64_t dodesc = sdesc_sw128(st + S::QT_BYTES, 16, 1024);   // dO_t as K-major B
                 if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
@@ -264,32 +272,38 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
                     tc_commit(bar(S::BAR_SFULL));
                 }
                 __syncwarp();
-                if (!wwait(bar(S::BAR_DSREADY), t & 1, 12)) break;
+                return true;
+            };
+            if (ok) ok = issue_a(0);
+            for (int t = 0; ok && t < nit; ++t) {
+                // step t+1's S^T, dP^T overwrite step t's once the warps hold them
+                if (t + 1 < nit) {
+                    if (!wwait(bar(S::BAR_SFREE), t & 1, 12) || !issue_a(t + 1)) break;
+                }
+                if (!wwait(bar(S::BAR_DSREADY), t & 1, 13)) break;
                 tc_fence_after();
+                const int slot = t % S::NS;
+                const uint32_t st = sRing + slot * S::STAGE_BYTES;
+                const uint64_t qdesc_mn = sdesc_sw128(st, BR * 128, 1024);              // Q_t as MN-major B
+                const uint64_t dodesc_mn = sdesc_sw128(st + S::QT_BYTES, BR * 128, 1024);
                 if (leader) {
-                    // K = BR query columns; warpgroup h wrote queries 32h .. 32h+31
-                    // as bf16 pairs into columns 32h .. 32h+15 of S^T (P^T) and dP^T (dS^T)
+                    // K = BR query columns: 16 queries = 8 columns of bf16 pairs
 #pragma unroll
-                    for (int kk = 0; kk < BR / 16; ++kk) {
-                        const uint32_t acol = (kk >> 1) * 32 + (kk & 1) * 8;
-                        mma_bf16_ts(tmem + S::C_DV, tmem + S::C_S + acol,
+                    for (int kk = 0; kk < BR / 16; ++kk)
+                        mma_bf16_ts(tmem + S::C_DV, tmem + S::C_P + 8 * kk,
                                     dodesc_mn + static_cast<uint64_t>((kk * 2048) >> 4), idesc_g,
                                     (t > 0 || kk > 0) ? 1u : 0u);
-                    }
 #pragma unroll
-                    for (int kk = 0; kk < BR / 16; ++kk) {
-                        const uint32_t acol = (kk >> 1) * 32 + (kk & 1) * 8;
-                        mma_bf16_ts(tmem + S::C_DK, tmem + S::C_DP + acol,
+                    for (int kk = 0; kk < BR / 16; ++kk)
+                        mma_bf16_ts(tmem + S::C_DK, tmem + S::C_DS + 8 * kk,
                                     qdesc_mn + static_cast<uint64_t>((kk * 2048) >> 4), idesc_g,
                                     (t > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    // dQ_i = dS K_j over K = BC keys (16 keys = 2048 bytes of both operands)
+                    // dQ_t^T = K^T dS^T over K = BC keys (16 keys = 2048 bytes of both operands)
 #pragma unroll
-                    for (int kk = 0; kk < BC / 16; ++kk) {
-                        mma_bf16_ss(tmem + S::C_DQ, dsdesc + static_cast<uint64_t>((kk * 2048) >> 4),
-                                    kdesc_mn + static_cast<uint64_t>((kk * 2048) >> 4), idesc_q, kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(bar(S::BAR_DQFULL));
+                    for (int kk = 0; kk < BC / 16; ++kk)
+                        mma_bf16_ss(tmem + S::C_DQ, ktdesc + static_cast<uint64_t>((kk * 2048) >> 4),
+                                    dsdesc + static_cast<uint64_t>((kk * 2048) >> 4), idesc_q, kk > 0 ? 1u : 0u);
+                    tc_commit(bar(S::BAR_BDONE));
                     tc_commit(bar(S::BAR_EMPTY + slot));
                 }
                 __syncwarp();
@@ -311,6 +325,25 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
         if (key >= N) mask2 = kNegInfBw;
         else if (p.key_mask) mask2 = __ldg(p.key_mask + static_cast<size_t>(bh) * N + key) * kLog2eBw;
         const float *stat = reinterpret_cast<const float *>(smem + S::OFF_STAT);
+        // dQ^T rows: lane = head-dim index c (M = 128), or lanes 0..15 of each
+        // warp (M = 64, rows 16 wq .. 16 wq + 15)
+        const bool dq_lane = (D == 128) || (lane < 16);
+        const int dq_c = (D == 128) ? wq * 32 + lane : wq * 16 + (lane & 15);
+        // Adds the dQ^T partial of step tq (queries (it0+tq)*BR + 32h + e) into the accumulator.
+        auto drain_dq = [&](int tq) {
+            uint32_t r[32];
+            tmem_ld32(tmem + t_lane + S::C_DQ + 32 * h, r);
+            tmem_ld_wait();
+            reg_fence32(r);
+            const int qb = (it0 + tq) * BR + 32 * h;
+            if (dq_lane) {
+                float *dst = p.dq_acc + (static_cast<size_t>(bh) * N + qb) * D + dq_c;
+                const int ne = min(32, N - qb);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (e < ne) atomicAdd(dst + static_cast<size_t>(e) * D, __uint_as_float(r[e]));
+            }
+        };
         bool ok = true;
         for (int t = 0; t < nit; ++t) {
             const int slot = t % S::NS;
@@ -326,6 +359,8 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
             tmem_ld_wait();
             reg_fence32(s);
             reg_fence32(dp);
+            tc_fence_before();
+            mbar_arrive(bar(S::BAR_SFREE));
             // this warpgroup's queries q0 + 32h + c
             const float *l2s = stat + slot * (S::STAT_BYTES / 4) + 32 * h;
             const float *dvs = l2s + BR;
@@ -346,9 +381,19 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
                 pk[e] = pack_bf16x2(pr[0], pr[1]);
                 dk[e] = pack_bf16x2(ds[0], ds[1]);
             }
-            tmem_st16(tmem + t_lane + S::C_S + 32 * h, pk);
-            tmem_st16(tmem + t_lane + S::C_DP + 32 * h, dk);
-            // dS into shared memory: row key_in of the MN-major tile (64 queries
+            // The previous step's products have read P^T, dS^T and the shared dS^T:
+            // add its dQ^T, then overwrite them.
+            if (t > 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(bar(S::BAR_BDONE), (t - 1) & 1, abort_flag, p.err, 21))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                drain_dq(t - 1);
+            }
+            tmem_st16(tmem + t_lane + S::C_P + 16 * h, pk);
+            tmem_st16(tmem + t_lane + S::C_DS + 16 * h, dk);
+            // dS^T into shared memory: row key_in of the MN-major tile (64 queries
             // = one 128-byte row, 16-byte chunks XOR-swizzled by key_in % 8);
             // this warpgroup's 32 queries are chunks 4h .. 4h+3.
             {
@@ -365,30 +410,10 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(S::BAR_DSREADY));
-            // dQ partial of this step: M = 64 accumulator, rows 16wq .. 16wq+15
-            // in lanes 0..15; warpgroup h adds columns h*D/2 .. (h+1)*D/2 - 1.
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(S::BAR_DQFULL), t & 1, abort_flag, p.err, 21))) {
-                ok = false;
-                break;
-            }
+        }
+        if (ok && __all_sync(0xffffffffu, mbar_wait(bar(S::BAR_BDONE), (nit - 1) & 1, abort_flag, p.err, 23))) {
             tc_fence_after();
-            const int qrow = q0 + 16 * wq + (lane & 15);
-            float *dst = p.dq_acc + (static_cast<size_t>(bh) * N + qrow) * D + h * (D / 2);
-#pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(tmem + t_lane + S::C_DQ + h * (D / 2) + 32 * cc, r);
-                tmem_ld_wait();
-                reg_fence32(r);
-                if (lane < 16 && qrow < N) {
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        atomicAdd(reinterpret_cast<float4 *>(dst + 32 * cc + 4 * v),
-                                  make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
-                }
-            }
-            tc_fence_before();
+            drain_dq(nit - 1);
         }
         (void)ok;
         // ---------------- epilogue: dV, scale * dK ----------------
