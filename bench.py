@@ -285,6 +285,87 @@ def run_decode(args):
     }))
 
 
+BWD_SHAPE = (2, 16, 4096, 128)   # B, H, N, d: the headline shape's backward, bf16, non-causal
+
+
+def run_bwd(args):
+    """Gradients of attention (attn_bwd) on the headline shape: one JSON line
+    with TFLOP/s over the five N x N x d products of the backward (10 B H N^2 d:
+    S recomputed, dP, dV, dK, dQ) against the measured bf16 peak.  The time is
+    the whole call (prep, main and finish launches).  ``--workload bwd``."""
+    import numpy as np
+    import exact_tiled_attention_17_gb300 as eta
+    import oracle
+    B, H, N, d = BWD_SHAPE
+    dev = torch.device("cuda", 0)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    sets = []   # two sets of 168 MB of inputs each: every step reads data not in L2
+    host0 = None
+    for s in range(2):
+        q, k, v = workloads.make_qkv(B, H, N, d, "bf16", seed=s)
+        do = workloads.make_grad_out(B, H, N, d, "bf16", seed=s)
+        if s == 0:
+            host0 = (q, k, v, do)
+        qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+        o, lse = eta.attn_fwd(qd, kd, vd, False, scale)
+        sets.append((qd, kd, vd, o, dod, lse))
+    dq, dk, dv = (torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    ws = torch.empty(eta.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        q, k, v, o, do, lse = sets[i % 2]
+        eta.attn_bwd(q, k, v, o, do, lse, False, scale, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    # parity before timing: two whole heads of set 0 against the FP64 gradient oracle
+    step(0)
+    torch.cuda.synchronize()
+    heads = [0, B * H - 1]
+    cores = oracle.default_threads()
+    t0 = time.perf_counter()
+    ref = oracle.attn_bwd(*host0[:3], host0[3], False, scale, heads=heads, nthreads=cores)
+    t_oracle = time.perf_counter() - t0
+    parity = {}
+    for name, got, want in (("dQ", dq, ref[0]), ("dK", dk, ref[1]), ("dV", dv, ref[2])):
+        g = got.reshape(B * H, N, d)[heads].double().cpu().numpy()
+        parity[name] = float(np.abs(g - want).max() / max(1.0, np.abs(want).max()))
+    clocks = ClockSampler(0)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = 10.0 * B * H * N * N * d
+    tflops = flops / ms / 1e9
+    pk = peaks()
+    print(json.dumps({
+        "metric": "attn bwd TFLOP/s (10*B*H*N^2*d: S recomputed, dP, dV, dK, dQ) and % of GB300 BF16 tensor peak",
+        "value": tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "bwd_bf16_2x16x4096x128", "B": B, "H": H, "N": N, "d": d, "causal": False,
+                   "l2": "2 rotating input sets of 168 MB (each step reads data not in L2)"},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tflops / pk["bf16_tflops"], "traffic": None,
+                     "peak_source": "measured bf16 burst" if pk["source"] == "measured" else "fallback",
+                     "timed": "whole attn_bwd call (prep + main + finish launches)"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": {"value": len(heads) * 10.0 * N * N * d / t_oracle / 1e12, "unit": "TFLOP/s",
+                         "cores": cores, "kind": "oracle",
+                         "sample": f"{len(heads)} whole heads of {B * H}, {t_oracle:.1f} s wall"},
+        "parity": {"heads": heads, "max_abs_over_max1_ref": parity, "tol": 2e-2},
+    }))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -294,14 +375,16 @@ def main():
     ap.add_argument("--Br", type=int, default=0)
     ap.add_argument("--Bc", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="attn", choices=["attn", "decode"],
+    ap.add_argument("--workload", default="attn", choices=["attn", "decode", "bwd"],
                     help="attn: the bf16 2x16x4096x128 forward (default); decode: attn_decode_fwd, 1x32 heads, "
-                         "one token against a 32768-long cache")
+                         "one token against a 32768-long cache; bwd: attn_bwd on 2x16x4096x128")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.workload == "decode":
         return run_decode(args)
+    if args.workload == "bwd":
+        return run_bwd(args)
     if args.impl == "reference":
         return run_reference(args)
 

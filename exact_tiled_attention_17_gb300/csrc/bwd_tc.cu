@@ -22,9 +22,9 @@
 //                        registers, and write P^T and dS^T (bf16) into their
 //                        own tensor-memory columns and dS^T into shared memory
 //                        (an operand of the dQ product).  Then the previous
-//                        step's dQ^T partial is added into the f32 accumulator
-//                        in global memory: lane = head-dim index, so each
-//                        warp-wide reduction covers one 128-byte line.
+//                        step's dQ^T partial goes to shared memory as dQ rows
+//                        and one bulk tensor reduction per warpgroup adds them
+//                        into the f32 accumulator in global memory.
 //            warp 8      TMA producer: K_j, V_j once; Q_i, dO_i tiles and the
 //                        step's LSE / D slices into a ring of NS stages.
 //            warp 9      MMA issuer: S^T = K Q_i^T and dP^T = V dO_i^T (both
@@ -51,6 +51,17 @@ constexpr float kLog2eBw = 1.4426950408889634f;
 constexpr float kNegInfBw = -__builtin_huge_valf();
 constexpr float kPosInfBw = __builtin_huge_valf();
 
+// Element-wise add of a shared-memory tile into global memory through a tensor
+// map (float32 here), as one bulk-group operation; rows outside the tensor are
+// dropped.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *m, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 template <int D>
 struct BwdShape {
     static constexpr int BR = 64;    // query rows per step (streamed)
@@ -61,12 +72,14 @@ struct BwdShape {
     static constexpr int STAGE_BYTES = 2 * QT_BYTES; // Q_i | dO_i
     static constexpr int STAT_BYTES = 2 * BR * 4;    // LSE (log2) | D of the step's rows
     static constexpr int DS_BYTES = BR * BC * 2;     // dS^T, MN-major B operand of K^T dS^T
-    static constexpr int NS = 4;
+    static constexpr int DQ_BYTES = BR * D * 4;      // dQ partial rows (f32), staged for the bulk reduction
+    static constexpr int NS = 3;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = KV_BYTES;
     static constexpr int OFF_RING = 2 * KV_BYTES;
     static constexpr int OFF_DS = OFF_RING + NS * STAGE_BYTES;
-    static constexpr int OFF_STAT = OFF_DS + DS_BYTES;
+    static constexpr int OFF_DQ = OFF_DS + DS_BYTES;
+    static constexpr int OFF_STAT = OFF_DQ + DQ_BYTES;
     static constexpr int OFF_BAR = OFF_STAT + NS * STAT_BYTES;
     // barriers: kv_full, full[NS], empty[NS], s_full, s_free, ds_ready, b_done, done
     static constexpr int BAR_KV = 0;
@@ -124,7 +137,7 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                       const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using S = BwdShape<D>;
     constexpr int BR = S::BR, BC = S::BC;
     extern __shared__ uint8_t smem_raw[];
@@ -156,6 +169,7 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
     const uint32_t sV = sbase + S::OFF_V;
     const uint32_t sRing = sbase + S::OFF_RING;
     const uint32_t sDS = sbase + S::OFF_DS;
+    const uint32_t sDQ = sbase + S::OFF_DQ;
     const uint32_t sStat = sbase + S::OFF_STAT;
 
     if (threadIdx.x == 0) {
@@ -329,29 +343,41 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
         // warp (M = 64, rows 16 wq .. 16 wq + 15)
         const bool dq_lane = (D == 128) || (lane < 16);
         const int dq_c = (D == 128) ? wq * 32 + lane : wq * 16 + (lane & 15);
-        // Adds the dQ^T partial of step tq (queries (it0+tq)*BR + 32h + e) into the accumulator.
-        auto drain_dq = [&](int tq) {
+        // One thread per warpgroup issues that warpgroup's bulk reductions.
+        const bool issuer = (wq == 0) && (lane == 0);
+        const uint32_t stage_dq = sDQ + h * (32 * D * 4);   // 32 query rows x D floats
+        // Adds the dQ^T partial of step tq (queries (it0+tq)*BR + 32h + e, e < 32)
+        // into the accumulator: the rows go to shared memory, then one bulk
+        // tensor reduction adds them (rows past N are dropped by the copy).
+        auto drain_dq = [&](int tq, bool live) {
             uint32_t r[32];
             tmem_ld32(tmem + t_lane + S::C_DQ + 32 * h, r);
             tmem_ld_wait();
             reg_fence32(r);
-            const int qb = (it0 + tq) * BR + 32 * h;
+            if (issuer) tma_store_wait_read0();   // the previous reduction has read the staging rows
+            named_bar_sync(2 + h, 128);
             if (dq_lane) {
-                float *dst = p.dq_acc + (static_cast<size_t>(bh) * N + qb) * D + dq_c;
-                const int ne = min(32, N - qb);
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                    if (e < ne) atomicAdd(dst + static_cast<size_t>(e) * D, __uint_as_float(r[e]));
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(stage_dq + (e * D + dq_c) * 4), "r"(r[e]) : "memory");
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(2 + h, 128);
+            const int y = (it0 + tq) * BR + 32 * h;
+            if (issuer && live && y < N) {
+                tma_reduce_add_3d(&tm_dq, stage_dq, 0, y, bh);
+                tma_store_commit();
             }
         };
+        // A wait that gives up (the error word records it; every later wait then
+        // gives up at once) does not end the loop: every warp still takes part
+        // in every named barrier, on whatever the buffers hold, and nothing is
+        // reduced into global memory.
         bool ok = true;
         for (int t = 0; t < nit; ++t) {
             const int slot = t % S::NS;
             const int q0 = (it0 + t) * BR;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(S::BAR_SFULL), t & 1, abort_flag, p.err, 20))) {
-                ok = false;
-                break;
-            }
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(S::BAR_SFULL), t & 1, abort_flag, p.err, 20)) && ok;
             tc_fence_after();
             uint32_t s[32], dp[32];
             tmem_ld32(tmem + t_lane + S::C_S + 32 * h, s);
@@ -361,9 +387,9 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
             reg_fence32(dp);
             tc_fence_before();
             mbar_arrive(bar(S::BAR_SFREE));
-            // this warpgroup's queries q0 + 32h + c
-            const float *l2s = stat + slot * (S::STAT_BYTES / 4) + 32 * h;
-            const float *dvs = l2s + BR;
+            // this warpgroup's queries q0 + 32h + c; lane c holds query c's LSE (log2) and D
+            const float *st_h = stat + slot * (S::STAT_BYTES / 4) + 32 * h;
+            const float my_l2 = st_h[lane], my_dv = st_h[BR + lane];
             const int qb = q0 + 32 * h;
             const bool diag = p.causal && (qb <= key0 + BC - 1);   // some query here precedes some key of the tile
             uint32_t pk[16], dk[16];
@@ -373,23 +399,20 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int c = 2 * e + u;
-                    float x = fmaf(__uint_as_float(s[c]), sl2, mask2) - l2s[c];
+                    float x = fmaf(__uint_as_float(s[c]), sl2, mask2) - __shfl_sync(0xffffffffu, my_l2, c);
                     if (diag && qb + c < key) x = kNegInfBw;
                     pr[u] = ex2(x);
-                    ds[u] = pr[u] * (__uint_as_float(dp[c]) - dvs[c]);
+                    ds[u] = pr[u] * (__uint_as_float(dp[c]) - __shfl_sync(0xffffffffu, my_dv, c));
                 }
                 pk[e] = pack_bf16x2(pr[0], pr[1]);
                 dk[e] = pack_bf16x2(ds[0], ds[1]);
             }
             // The previous step's products have read P^T, dS^T and the shared dS^T:
-            // add its dQ^T, then overwrite them.
+            // reduce its dQ^T, then overwrite them.
             if (t > 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(bar(S::BAR_BDONE), (t - 1) & 1, abort_flag, p.err, 21))) {
-                    ok = false;
-                    break;
-                }
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(S::BAR_BDONE), (t - 1) & 1, abort_flag, p.err, 21)) && ok;
                 tc_fence_after();
-                drain_dq(t - 1);
+                drain_dq(t - 1, ok);
             }
             tmem_st16(tmem + t_lane + S::C_P + 16 * h, pk);
             tmem_st16(tmem + t_lane + S::C_DS + 16 * h, dk);
@@ -411,11 +434,10 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
             tc_fence_before();
             mbar_arrive(bar(S::BAR_DSREADY));
         }
-        if (ok && __all_sync(0xffffffffu, mbar_wait(bar(S::BAR_BDONE), (nit - 1) & 1, abort_flag, p.err, 23))) {
-            tc_fence_after();
-            drain_dq(nit - 1);
-        }
-        (void)ok;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(S::BAR_BDONE), (nit - 1) & 1, abort_flag, p.err, 23)) && ok;
+        tc_fence_after();
+        drain_dq(nit - 1, ok);
+        if (issuer) tma_store_wait0();   // every reduction of this warpgroup has completed
         // ---------------- epilogue: dV, scale * dK ----------------
         mbar_wait(bar(S::BAR_DONE), 0, abort_flag, p.err, 22);
         tc_fence_after();
@@ -531,6 +553,20 @@ bool make_rows_map(CUtensorMap *m, const void *base, int D, int N, int BH, int b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The float32 dQ accumulator [BH][N][D] as a tensor of 32-row boxes (no swizzle).
+bool make_acc_map(CUtensorMap *m, const float *base, int D, int N, int BH) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(N) * D * 4};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 32u, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int npad_of(int N) { return (N + 63) / 64 * 64; }
@@ -555,10 +591,11 @@ int launch_bwd_d(const void *Q, const void *K, const void *V, const void *O, con
     float *dvec = reinterpret_cast<float *>(ws + round256(static_cast<size_t>(BH) * npad * 4));
     float *acc = reinterpret_cast<float *>(ws + 2 * round256(static_cast<size_t>(BH) * npad * 4));
 
-    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
     if (!make_rows_map(&tq, Q, D, N, BH, S::BR) || !make_rows_map(&tk, K, D, N, BH, S::BC) ||
         !make_rows_map(&tv, V, D, N, BH, S::BC) || !make_rows_map(&tdo, dO, D, N, BH, S::BR) ||
-        !make_rows_map(&tdk, dK, D, N, BH, S::BC) || !make_rows_map(&tdv, dV, D, N, BH, S::BC))
+        !make_rows_map(&tdk, dK, D, N, BH, S::BC) || !make_rows_map(&tdv, dV, D, N, BH, S::BC) ||
+        !make_acc_map(&tdq, acc, D, N, BH))
         return kErrCuda;
     int *err = device_error_word();
     if (!err) return kErrCuda;
@@ -588,7 +625,7 @@ int launch_bwd_d(const void *Q, const void *K, const void *V, const void *O, con
     p.err = err;
     const long long grid = static_cast<long long>(BH) * p.nkt;
     if (grid > 0x7fffffffLL) return kErrUnsupported;
-    kern<<<static_cast<unsigned>(grid), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
+    kern<<<static_cast<unsigned>(grid), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p);
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     {
         const long long n4 = static_cast<long long>(BH) * N * D / 4;
