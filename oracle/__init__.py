@@ -8,10 +8,12 @@ arrays into it.
 
 Functions
 ---------
-attn(q, k, v, causal, scale, key_mask=None, rows=None)
+attn(q, k, v, causal, scale, key_mask=None, rows=None, block_mask=None, block=(128, 128))
     The definition of attention, softmax(Q K^T * scale + mask) V, one row at
     a time in binary64 ("Is Flash Attention Stable?" §II-A, the
     Attention(Q,K,V) equation).  Fully masked rows give O = 0, LSE = -inf.
+    ``block_mask`` ([..., ceil(N/bq), ceil(N/bk)], non-zero = take part) sets
+    every score outside the marked blocks to -inf: the block-sparse reading.
 blocked_row(scores, values, width, block_order=None, no_rescale=False)
     The online merge of one row of scores, block by block, with the running
     maximum / denominator / unnormalised-vector state of the yadro-code.ru
@@ -77,6 +79,11 @@ def _load():
                                                  ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                                  lp, ctypes.c_longlong, dp, dp, ctypes.c_int]
             lib.oracle_attn_rows_f64.restype = ctypes.c_int
+            ubp = ctypes.POINTER(ctypes.c_ubyte)
+            lib.oracle_attn_rows_bs_f64.argtypes = [dp, dp, dp, dp, ubp, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_double, lp, ctypes.c_longlong, dp, dp, ctypes.c_int]
+            lib.oracle_attn_rows_bs_f64.restype = ctypes.c_int
             ip = ctypes.POINTER(ctypes.c_int)
             lib.oracle_blocked_row_f64.argtypes = [dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    ip, ctypes.c_int, dp, dp]
@@ -117,7 +124,8 @@ def default_threads() -> int:
     return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
 
 
-def attn(q, k, v, causal: bool, scale: float, key_mask=None, rows=None, nthreads: int | None = None):
+def attn(q, k, v, causal: bool, scale: float, key_mask=None, rows=None, nthreads: int | None = None,
+         block_mask=None, block=(128, 128)):
     """Binary64 attention.
 
     q, k, v: [..., N, d] (leading dims flattened to BH); key_mask: None or
@@ -144,12 +152,20 @@ def attn(q, k, v, causal: bool, scale: float, key_mask=None, rows=None, nthreads
     else:
         R = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         nrows = R.size
+    BM = None
+    bq, bk = int(block[0]), int(block[1])
+    if block_mask is not None:
+        bm = block_mask.detach().cpu().numpy() if hasattr(block_mask, "detach") else np.asarray(block_mask)
+        BM = np.ascontiguousarray((bm != 0).astype(np.uint8))
+        if BM.size != BH * ((N + bq - 1) // bq) * ((N + bk - 1) // bk):
+            raise ValueError("block_mask must have BH * ceil(N/bq) * ceil(N/bk) elements")
     O = np.zeros((nrows, d), dtype=np.float64)
     L = np.zeros((nrows,), dtype=np.float64)
-    rc = lib.oracle_attn_rows_f64(_ptr(Q), _ptr(K), _ptr(V), _ptr(M) if M is not None else None,
-                                  BH, N, d, 1 if causal else 0, float(scale),
-                                  _ptr(R, ctypes.c_longlong) if R is not None else None, nrows,
-                                  _ptr(O), _ptr(L), nthreads or default_threads())
+    rc = lib.oracle_attn_rows_bs_f64(_ptr(Q), _ptr(K), _ptr(V), _ptr(M) if M is not None else None,
+                                     _ptr(BM, ctypes.c_ubyte) if BM is not None else None, bq, bk,
+                                     BH, N, d, 1 if causal else 0, float(scale),
+                                     _ptr(R, ctypes.c_longlong) if R is not None else None, nrows,
+                                     _ptr(O), _ptr(L), nthreads or default_threads())
     if rc != 0:
         raise RuntimeError("oracle_attn_rows_f64 failed")
     if rows is None:

@@ -23,6 +23,15 @@
  *    it is defined as O = 0, LSE = -inf.  LSE is the natural-log
  *    log-sum-exp of the row's scaled, masked scores.
  *
+ *  oracle_attn_rows_bs_f64 — the same definition with a block mask: the
+ *    yadro-code.ru tutorial mentions that the method's paper also treats a
+ *    block-sparse extension; read plainly, a block mask marks which
+ *    (query block, key block) pairs of the score matrix take part, and every
+ *    score outside the marked blocks is -inf before the softmax (a block row
+ *    with no marked block is a fully masked row).  Blocks are `bq` query rows
+ *    by `bk` keys; the mask is [BH][ceil(N/bq)][ceil(N/bk)] bytes, non-zero =
+ *    take part.
+ *
  *  oracle_blocked_row_f64 — the online merge for one row of scores,
  *    following the same tutorial's description of the running state
  *    (maximum m, denominator l, unnormalised vector a): when a block with a
@@ -56,6 +65,8 @@
 
 typedef struct {
     const double *Q, *K, *V, *mask;
+    const unsigned char *bmask; /* NULL, or [BH][ceil(N/bq)][ceil(N/bk)] */
+    int bq, bk;
     int N, d, causal;
     double scale;
     const long long *rows; /* NULL: rows 0 .. nrows-1 */
@@ -75,11 +86,15 @@ static void direct_row(const rows_job_t *job, long long flat, double *s, double 
     const double *Kh = job->K + bh * (long long)N * d;
     const double *Vh = job->V + bh * (long long)N * d;
     const double *mk = job->mask ? job->mask + bh * (long long)N : NULL;
+    const int nqb = job->bmask ? (N + job->bq - 1) / job->bq : 0;
+    const int nkb = job->bmask ? (N + job->bk - 1) / job->bk : 0;
+    const unsigned char *brow = job->bmask ? job->bmask + ((long long)bh * nqb + i / job->bq) * nkb : NULL;
 
     /* scores s_j = scale * <q_i, k_j> + mask_j, -inf where not allowed */
     double m = -INFINITY;
     for (int j = 0; j < N; ++j) {
         if (job->causal && j > i) { s[j] = -INFINITY; continue; }
+        if (brow && !brow[j / job->bk]) { s[j] = -INFINITY; continue; }
         double dot = 0.0;
         const double *kj = Kh + (long long)j * d;
         for (int c = 0; c < d; ++c) dot += q[c] * kj[c];
@@ -134,11 +149,28 @@ static void *rows_worker(void *arg)
  * LSE [BH*N]), else `nrows` flat row ids bh*N + i (O is [nrows][d]).
  * Returns 0, or -1 on bad arguments / allocation failure.
  */
+int oracle_attn_rows_bs_f64(const double *Q, const double *K, const double *V,
+                            const double *key_mask, const unsigned char *block_mask, int bq, int bk,
+                            int BH, int N, int d, int causal, double scale,
+                            const long long *rows, long long nrows, double *O, double *LSE, int nthreads);
+
 int oracle_attn_rows_f64(const double *Q, const double *K, const double *V,
                          const double *key_mask, int BH, int N, int d, int causal,
                          double scale, const long long *rows, long long nrows,
                          double *O, double *LSE, int nthreads)
 {
+    return oracle_attn_rows_bs_f64(Q, K, V, key_mask, NULL, 1, 1, BH, N, d, causal, scale, rows, nrows,
+                                   O, LSE, nthreads);
+}
+
+/* As oracle_attn_rows_f64, with an optional block mask (NULL: none) of
+ * bq x bk blocks. */
+int oracle_attn_rows_bs_f64(const double *Q, const double *K, const double *V,
+                            const double *key_mask, const unsigned char *block_mask, int bq, int bk,
+                            int BH, int N, int d, int causal, double scale,
+                            const long long *rows, long long nrows, double *O, double *LSE, int nthreads)
+{
+    if (block_mask && (bq <= 0 || bk <= 0)) return -1;
     if (!Q || !K || !V || !O || !LSE || BH <= 0 || N <= 0 || d <= 0) return -1;
     if (!rows) nrows = (long long)BH * N;
     for (long long r = 0; rows && r < nrows; ++r)
@@ -146,6 +178,7 @@ int oracle_attn_rows_f64(const double *Q, const double *K, const double *V,
     rows_job_t job;
     memset(&job, 0, sizeof(job));
     job.Q = Q; job.K = K; job.V = V; job.mask = key_mask;
+    job.bmask = block_mask; job.bq = bq; job.bk = bk;
     job.N = N; job.d = d; job.causal = causal; job.scale = scale;
     job.rows = rows; job.nrows = nrows; job.O = O; job.LSE = LSE;
     pthread_mutex_init(&job.lock, NULL);
