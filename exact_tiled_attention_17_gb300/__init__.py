@@ -31,7 +31,7 @@ ATTN_ERR_CUDA = -4
 ATTN_ERR_DEVICE_TIMEOUT = -5
 
 # Every symbol include/attn.h declares.
-EXPORTS = ("attn_fwd", "attn_naive_workspace_size", "attn_naive_fwd", "attn_deviation_workspace_size",
+EXPORTS = ("attn_fwd", "attn_fwd_block_sparse", "attn_naive_workspace_size", "attn_naive_fwd", "attn_deviation_workspace_size",
            "attn_deviation", "attn_deviation_noalloc", "attn_decode_workspace_size", "attn_decode_fwd",
            "attn_bwd_workspace_size", "attn_bwd", "attn_emul_fwd", "attn_emul_round", "attn_status",
            "attn_strerror", "attn_last_variant", "attn_debug_wait_timeout")
@@ -58,6 +58,8 @@ def _load() -> ctypes.CDLL:
     lib = ctypes.CDLL(LIB_PATH)
     vp, i, f, sz, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_longlong
     lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, vp, vp]
+    lib.attn_fwd_block_sparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp]
+    lib.attn_fwd_block_sparse.restype = i
     lib.attn_fwd.restype = i
     lib.attn_naive_workspace_size.argtypes = [i, i, i, i]
     lib.attn_naive_workspace_size.restype = sz
@@ -120,6 +122,46 @@ def _shape4(q):
     if q.dim() == 3:
         return (1,) + tuple(q.shape)
     raise ValueError("q, k, v must be [B, H, N, d] or [H, N, d]")
+
+
+BLOCK_SPARSE_BLOCK = 128
+BLOCK_SPARSE_MAX_N = 131072
+
+
+def attn_fwd_block_sparse(q, k, v, block_mask, causal: bool = False, scale: float | None = None, key_mask=None,
+                          out=None, lse=None, stream=None, want_lse: bool = True):
+    """Forward restricted to the marked 128 x 128 blocks.  block_mask: [B, H,
+    nb, nb] uint8 (or bool) device tensor, nb = ceil(N / 128), non-zero = the
+    block takes part.  Returns (o, lse)."""
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous device tensors")
+    if not (q.shape == k.shape == v.shape and q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share shape and dtype")
+    B, H, N, d = _shape4(q)
+    nb = -(-N // BLOCK_SPARSE_BLOCK)
+    if block_mask.dtype == torch.bool:
+        block_mask = block_mask.to(torch.uint8)
+    if (block_mask.dtype != torch.uint8 or not block_mask.is_cuda or not block_mask.is_contiguous()
+            or block_mask.numel() != B * H * nb * nb):
+        raise ValueError("block_mask must be a contiguous uint8 device tensor with B*H*nb*nb elements")
+    if q.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = out if out is not None else torch.empty_like(q)
+    l = lse if lse is not None else (torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+                                     if want_lse else None)
+    m = None
+    if key_mask is not None:
+        m = key_mask
+        if m.dtype != torch.float32 or not m.is_contiguous() or m.numel() != B * H * N or not m.is_cuda:
+            raise ValueError("key_mask must be a contiguous float32 device tensor with B*H*N elements")
+    rc = lib.attn_fwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, int(bool(causal)),
+                                   float(scale), _DTYPE[q.dtype], _ptr(block_mask), _ptr(m),
+                                   ctypes.c_void_p(_stream(stream)))
+    _check(rc, "attn_fwd_block_sparse")
+    return o, l
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, Br: int = 0, Bc: int = 0,

@@ -127,6 +127,33 @@ int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, i
     return rc;
 }
 
+int attn_fwd_block_sparse(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
+                          int d, int causal, float scale, int dtype, const unsigned char *block_mask,
+                          const float *key_mask, void *stream) {
+    int rc = check_common(Q, K, V, O, B, H, N, d, scale, key_mask);
+    if (rc != kOk) return rc;
+    if (!block_mask) return kErrArg;
+    if (causal != 0 && causal != 1) return kErrArg;
+    if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return kErrArg;
+    if (dtype != ATTN_BF16) return (dtype == ATTN_F32 || dtype == ATTN_F64) ? kErrUnsupported : kErrArg;
+    if (d != 64 && d != 128) return kErrUnsupported;
+    if (N > ATTN_BLOCK_SPARSE_MAX_N) return kErrUnsupported;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return kErrCuda;
+    if (major != 10 || minor != 3) return kErrUnsupported;  // built for sm_103a only
+    const char *variant = "";
+    rc = launch_fwd_tc_bf16_bsparse(Q, K, V, O, LSE, B, H, N, d, causal, scale, block_mask, key_mask,
+                                    static_cast<cudaStream_t>(stream), &variant);
+    if (rc == kOk) t_last_variant = variant;
+    return rc;
+}
+
+static_assert(ATTN_BLOCK_SPARSE_BLOCK == eta::kBlockSparseBlock && ATTN_BLOCK_SPARSE_MAX_N == eta::kBlockSparseMaxN,
+              "header and library agree on the block-sparse limits");
+
 size_t attn_naive_workspace_size(int B, int H, int N, int dtype) {
     if (B <= 0 || H <= 0 || N <= 0) return 0;
     size_t es = dtype == ATTN_F32 ? 4 : dtype == ATTN_BF16 ? 2 : 0;

@@ -41,6 +41,12 @@
 // The two warpgroups of a tile take this decision together.
 // One denominator per row, the float32 sum of p: it normalises O (whose P V
 // uses p rounded to bf16) and gives the LSE.
+//
+// Block-sparse variant (BSPARSE): a byte mask over 128 x 128 (query block, key
+// block) pairs says which blocks take part; every other score is -inf.  The
+// CTA runs only the key tiles marked for at least one of its query tiles (a
+// list built at the start); a listed tile that is not marked for a query tile
+// is masked whole for it.
 #include <cuda_bf16.h>
 #include <type_traits>
 #include <cstdio>
@@ -59,7 +65,9 @@ constexpr float kRescaleThresh = 8.0f;
 constexpr float kFastSumLimit = 65536.0f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
-template <int D, int BR, int BC, int NQ, bool MASKED>
+constexpr int kBsListCap = 1024;   // key tiles a block-sparse CTA can list (N <= 131072)
+
+template <int D, int BR, int BC, int NQ, bool MASKED, bool BSPARSE = false>
 struct TcShape {
     static constexpr int CB = D / 64;               // 128-byte column blocks per row
     static constexpr int Q_BYTES = BR * D * 2;      // one Q (or O staging) tile
@@ -78,7 +86,9 @@ struct TcShape {
     static constexpr int NH = BC == 128 ? 2 : 1;
     // two warpgroups per tile exchange per-row values (half maxima, partial sums)
     static constexpr int XCH_BYTES = NH == 2 ? NQ * 2 * 128 * 8 : 0;
-    static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES - MASK_BYTES - XCH_BYTES) / SLOT_BYTES;
+    // block-sparse: the listed key tiles (index | per-query-tile marks << 14) and per-tile counts
+    static constexpr int LIST_BYTES = BSPARSE ? kBsListCap * 2 + 16 : 0;
+    static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES - MASK_BYTES - XCH_BYTES - LIST_BYTES) / SLOT_BYTES;
     static constexpr int NS = NS_RAW > 8 ? 8 : (NS_RAW < 2 ? 2 : NS_RAW);
     static constexpr int TMEM_USED = NQ * (NSB * BC + D);
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32
@@ -107,7 +117,8 @@ struct TcShape {
     static constexpr int OFF_RING = NQ * Q_BYTES;
     static constexpr int OFF_MASK = OFF_RING + NS * SLOT_BYTES;
     static constexpr int OFF_XCH = OFF_MASK + MASK_BYTES;
-    static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
+    static constexpr int OFF_LIST = OFF_XCH + XCH_BYTES;
+    static constexpr int OFF_BAR = OFF_LIST + LIST_BYTES;
     // barriers: q_full[NQ] full[NS] empty[NS] s_full[NQ][NSB] p_full[NQ][NSB][NH] o_full[NQ]
     // pv_done[NQ] done part done_read
     static constexpr int BAR_QFULL = 0;
@@ -145,7 +156,8 @@ struct TcShape {
                   "register split must equal the launch allocation");
     // two S buffers: K_{j+2} is waited for while V_j still holds its slot
     static_assert(!DBS || NS >= 4, "ring depth for two S buffers");
-    static constexpr bool CAN_SPLIT = (PART_BYTES <= NQ * Q_BYTES + NS * SLOT_BYTES) && (BR == 128);
+    static constexpr bool CAN_SPLIT = (PART_BYTES <= NQ * Q_BYTES + NS * SLOT_BYTES) && (BR == 128) && !BSPARSE;
+    static_assert(!BSPARSE || (BR == 128 && BC == 128 && NQ <= 2), "block-sparse tiles are the 128 x 128 blocks");
 };
 
 struct TcParams {
@@ -155,6 +167,8 @@ struct TcParams {
     int causal;
     float scale_log2;   // scale * log2(e)
     const float *key_mask;  // [BH][N] additive, or null
+    const uint8_t *block_mask;  // block-sparse: [BH][nkb][nkb] bytes, non-zero = take part
+    int nkb;                    // 128-row blocks per head
     float *lse;             // [BH][N], or null
     int *err;               // device error word
     // Work items (groups of NQ query tiles) are numbered in launch order.
@@ -164,12 +178,12 @@ struct TcParams {
     int split;
 };
 
-template <int D, int BR, int BC, int NQ, bool MASKED>
-__global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
+template <int D, int BR, int BC, int NQ, bool MASKED, bool BSPARSE>
+__global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                        const TcParams p) {
-    using S = TcShape<D, BR, BC, NQ, MASKED>;
+    using S = TcShape<D, BR, BC, NQ, MASKED, BSPARSE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -240,10 +254,71 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
         tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
         tmem_relinquish();
     }
+    uint16_t *kv_list = reinterpret_cast<uint16_t *>(smem + S::OFF_LIST);
+    if constexpr (BSPARSE) {
+        // Warp 1 lists the key tiles marked for at least one of the CTA's query
+        // tiles (in order, with the per-tile marks in bits 14..15) and, per
+        // query tile, how many list entries reach its last marked tile.  A
+        // query tile inside N with no marked tile still runs one fully masked
+        // tile, which writes O = 0 and LSE = -inf.
+        if (warp == 1) {
+            int *counts = reinterpret_cast<int *>(smem + S::OFF_LIST + kBsListCap * 2);
+            const int nkb = p.nkb;
+            const uint8_t *bm = p.block_mask + static_cast<size_t>(bh) * nkb * nkb;
+            int cnt = 0, last[NQ];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) last[q] = 0;
+            for (int j0 = 0; j0 < nkb; j0 += 32) {
+                const int jt = j0 + lane;
+                uint32_t marks = 0;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    if (r0[q] < N && jt < nkb) {
+                        bool a = bm[static_cast<size_t>(r0[q] / 128) * nkb + jt] != 0;
+                        if (p.causal) a = a && (jt * BC <= min(r0[q] + BR - 1, N - 1));
+                        if (a) marks |= 1u << q;
+                    }
+                }
+                const uint32_t ball = __ballot_sync(0xffffffffu, marks != 0);
+                if (marks) kv_list[cnt + __popc(ball & ((1u << lane) - 1u))] = static_cast<uint16_t>(jt | (marks << 14));
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const uint32_t bq = __ballot_sync(0xffffffffu, (marks >> q) & 1u);
+                    if (bq) {
+                        const int L = 31 - __clz(bq);
+                        last[q] = cnt + __popc(ball & ((1u << L) - 1u)) + 1;
+                    }
+                }
+                cnt += __popc(ball);
+            }
+            bool empty_tile = false;
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) empty_tile = empty_tile || (r0[q] < N && last[q] == 0);
+            if (empty_tile && cnt == 0 && lane == 0) kv_list[0] = 0;
+            if (lane == 0) {
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) counts[q] = (r0[q] < N && last[q] == 0) ? 1 : last[q];
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if constexpr (BSPARSE) {
+        const int *counts = reinterpret_cast<const int *>(smem + S::OFF_LIST + kBsListCap * 2);
+        nkv_max = 0;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            nkv[q] = counts[q];
+            nkv_max = max(nkv_max, nkv[q]);
+        }
+    }
+    // first key of the CTA's j-th K/V tile
+    auto kv_tile = [&](int jj) -> int {
+        if constexpr (BSPARSE) return kv_list[jj] & 0x3FFF;
+        else return kv_lo + jj;
+    };
     if constexpr (S::CAN_SPLIT) {
         // Parts of a split item arrive on each other's barriers: all of the
         // cluster's barriers must be initialised first.
@@ -295,7 +370,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
 #pragma unroll
                     for (int cb = 0; cb < S::CB; ++cb)
                         tma_load_3d_hint(sRing + slot * S::SLOT_BYTES + cb * (BC * 128), m,
-                                         bar(S::BAR_FULL + slot), cb * 64, (kv_lo + j) * BC, bh, pol_kv);
+                                         bar(S::BAR_FULL + slot), cb * 64, kv_tile(j) * BC, bh, pol_kv);
                 }
                 issued = t + 1;
             }
@@ -509,10 +584,13 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
             if (!mbar_wait(bar(S::BAR_SFULL + q * S::NSB + sb), (j / S::NSB) & 1, abort_flag, p.err, 20)) ok = false;
             tc_fence_after();
             const uint32_t tS = tmem + t_lane + S::s_col(q, sb);
-            const int key0 = (kv_lo + j) * BC;
+            const int key0 = kv_tile(j) * BC;
+            // block-sparse: a listed tile not marked for this query tile is masked whole
+            bool dead = false;
+            if constexpr (BSPARSE) dead = !((kv_list[j] >> (14 + q)) & 1);
             // Tiles that need per-element masking: the N tail, the causal
             // diagonal, or any tile when a key mask is given.
-            const bool edge = MASKED || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0q);
+            const bool edge = MASKED || dead || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0q);
 
             const bool diag = p.causal && key0 + BC - 1 > r0q;   // tile crosses the causal diagonal
             // Key mask of this warpgroup's columns, in log2 units with -inf
@@ -540,6 +618,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED>::THREADS, 1)
                         x = (key < N) ? __uint_as_float(r[e]) * sl2 : kNegInf;
                     }
                     if (diag) x = (key <= row) ? x : kNegInf;
+                    if constexpr (BSPARSE) x = dead ? kNegInf : x;
                     r[e] = __float_as_uint(x);
                 }
             };
@@ -970,11 +1049,12 @@ int sm_count(int dev) {
     return counts[dev];
 }
 
-template <int D, int BR, int BC, int NQ, bool MASKED>
+template <int D, int BR, int BC, int NQ, bool MASKED, bool BSPARSE = false>
 int launch_variant(const void *Q, const void *K, const void *V, void *O, float *LSE, int BH, int N,
-                   int causal, float scale, const float *key_mask, cudaStream_t stream, int *split_out) {
-    using S = TcShape<D, BR, BC, NQ, MASKED>;
-    auto kern = attn_fwd_tc_kernel<D, BR, BC, NQ, MASKED>;
+                   int causal, float scale, const float *key_mask, cudaStream_t stream, int *split_out,
+                   const uint8_t *block_mask = nullptr) {
+    using S = TcShape<D, BR, BC, NQ, MASKED, BSPARSE>;
+    auto kern = attn_fwd_tc_kernel<D, BR, BC, NQ, MASKED, BSPARSE>;
     static int attr_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
@@ -1001,6 +1081,8 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
     p.causal = causal;
     p.scale_log2 = scale * kLog2e;
     p.key_mask = key_mask;
+    p.block_mask = block_mask;
+    p.nkb = (N + 127) / 128;
     p.lse = LSE;
     p.err = device_error_word();
     if (!p.err) return kErrCuda;
@@ -1081,6 +1163,30 @@ int launch_br(int Bc, const void *Q, const void *K, const void *V, void *O, floa
 }
 
 }  // namespace
+
+int launch_fwd_tc_bf16_bsparse(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                               int N, int d, int causal, float scale, const uint8_t *block_mask,
+                               const float *key_mask, cudaStream_t stream, const char **variant) {
+    const int BH = B * H;
+    int split = 1;
+    int rc;
+    if (d == 128) {
+        rc = key_mask ? launch_variant<128, 128, 128, 2, true, true>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask,
+                                                                     stream, &split, block_mask)
+                      : launch_variant<128, 128, 128, 2, false, true>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask,
+                                                                      stream, &split, block_mask);
+        if (variant) *variant = key_mask ? "tc_bf16_d128_br128_bc128_nq2_mask_bsparse" : "tc_bf16_d128_br128_bc128_nq2_bsparse";
+    } else if (d == 64) {
+        rc = key_mask ? launch_variant<64, 128, 128, 2, true, true>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask,
+                                                                    stream, &split, block_mask)
+                      : launch_variant<64, 128, 128, 2, false, true>(Q, K, V, O, LSE, BH, N, causal, scale, key_mask,
+                                                                     stream, &split, block_mask);
+        if (variant) *variant = key_mask ? "tc_bf16_d64_br128_bc128_nq2_mask_bsparse" : "tc_bf16_d64_br128_bc128_nq2_bsparse";
+    } else {
+        return kErrUnsupported;
+    }
+    return rc;
+}
 
 int launch_fwd_tc_bf16(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
                        int d, int causal, float scale, int Br, int Bc, const float *key_mask,

@@ -35,6 +35,13 @@ int launch_fwd_tc_bf16(const void *Q, const void *K, const void *V, void *O, flo
                        int N, int d, int causal, float scale, int Br, int Bc, const float *key_mask,
                        cudaStream_t stream, const char **variant);
 
+// Block-sparse BF16 forward (fwd_tc.cu): 128 x 128 blocks, block_mask [B*H][nb][nb] bytes.
+constexpr int kBlockSparseBlock = 128;
+constexpr int kBlockSparseMaxN = 131072;
+int launch_fwd_tc_bf16_bsparse(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                               int N, int d, int causal, float scale, const unsigned char *block_mask,
+                               const float *key_mask, cudaStream_t stream, const char **variant);
+
 // FP32 tiled forward on the CUDA cores (fwd_f32.cu).
 int launch_fwd_f32(const float *Q, const float *K, const float *V, float *O, float *LSE, int B, int H,
                    int N, int d, int causal, float scale, const float *key_mask, cudaStream_t stream,

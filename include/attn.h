@@ -81,6 +81,28 @@ int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
              int dtype, const float *key_mask, void *stream);
 
 /*
+ * attn_fwd_block_sparse — the forward of attn_fwd restricted to marked blocks
+ * of the score matrix.  The yadro-code.ru FlashAttention tutorial notes that
+ * the method's paper also treats a block-sparse extension; read plainly, a
+ * block mask says which (query block, key block) pairs take part, every other
+ * score is -inf before the softmax, and the kernel skips the key tiles no
+ * query tile of a CTA needs.  A query row whose blocks are all unmarked (or
+ * that sees no allowed key inside them) gets O = 0, LSE = -inf.
+ *
+ * block_mask: [B][H][nb][nb] bytes, nb = ceil(N / ATTN_BLOCK_SPARSE_BLOCK),
+ * device memory, non-zero = the block takes part; block (i, j) covers query
+ * rows 128i .. 128i+127 and keys 128j .. 128j+127.  Other arguments as
+ * attn_fwd (key_mask and causal apply on top of the block mask).  dtype must
+ * be ATTN_BF16, d 64 or 128 and N <= ATTN_BLOCK_SPARSE_MAX_N, else
+ * ATTN_ERR_UNSUPPORTED; block_mask NULL is ATTN_ERR_ARG.  Asynchronous.
+ */
+#define ATTN_BLOCK_SPARSE_BLOCK 128
+#define ATTN_BLOCK_SPARSE_MAX_N 131072
+int attn_fwd_block_sparse(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                          int B, int H, int N, int d, int causal, float scale, int dtype,
+                          const unsigned char *block_mask, const float *key_mask, void *stream);
+
+/*
  * attn_naive_workspace_size — bytes of workspace attn_naive_fwd needs:
  * B*H*N*N elements of the input dtype (the materialised score matrix; the
  * tutorial's arithmetic: 8192 tokens x 2 bytes = 128 MiB per head, 4 GiB for

@@ -99,6 +99,28 @@ def make_grad_out(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int
     return do.to(TORCH_DTYPE[dtype]).contiguous()
 
 
+def make_block_mask(B: int, H: int, N: int, density: float = 0.5, seed: int = 0, pattern: str = "random",
+                    window: int = 2, block: int = 128):
+    """Block mask for the block-sparse forward, uint8 [B][H][nb][nb], nb =
+    ceil(N / block), 1 = the (query block, key block) pair takes part.
+
+    "random": each pair marked independently with probability ``density``
+    (seed + 4 stream).  "local": query block i marks key blocks within
+    ``window`` of i plus key block 0 (a sliding window with one global block),
+    the same for every head."""
+    nb = -(-N // block)
+    if pattern == "random":
+        g = torch.Generator(device="cpu").manual_seed(seed + 4)
+        m = (torch.rand((B, H, nb, nb), generator=g) < density).to(torch.uint8)
+    elif pattern == "local":
+        i = torch.arange(nb)
+        band = ((i[:, None] - i[None, :]).abs() <= window) | (i[None, :] == 0)
+        m = band.to(torch.uint8).expand(B, H, nb, nb).clone()
+    else:
+        raise ValueError(pattern)
+    return m.contiguous()
+
+
 def make_key_mask(B: int, H: int, N: int, frac: float, seed: int = 0,
                   force_masked_heads_every: int = 4, force_masked_keys: int = 4):
     """Additive key-padding mask, float32 [B][H][N], entries 0 or -inf.
