@@ -135,18 +135,27 @@ def dist_setup(n_gpus: int):
     return 0, 1, 0, None
 
 
-def barrier(dist):
+def barrier(dist, cuda: bool = True):
+    """All ranks meet (when there are several), then this rank's GPU work is done."""
     if dist is not None:
         dist.barrier()
-    torch.cuda.synchronize()
+    if cuda:
+        torch.cuda.synchronize()
 
 
-def max_over_ranks(dist, x: float) -> float:
+def max_over_ranks(dist, x: float, device: str = "cuda") -> float:
+    """The largest of the ranks' values of x (the slowest rank's time)."""
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of `flops_per_step`
+    (independent replicas), divided by the slowest rank's time."""
+    return flops_per_step * steps * world / (max_ms / 1e3) / 1e12
 
 
 def cpu_baseline(w, q, k, v, o_dev, target_s: float = 12.0):
@@ -536,7 +545,7 @@ def main():
     avg_kernel_ms = sum(kern_ms) / len(kern_ms)
 
     flops_step = w.flops
-    value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
+    value = whole_job_tflops(flops_step, args.steps, world, total_ms)
     pk = peaks()
     achieved = flops_step / (avg_kernel_ms / 1e3) / 1e12
 
@@ -556,7 +565,7 @@ def main():
     e1.record(stream)
     barrier(dist)
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
-    e2e_value = flops_step * e2e_steps * world / (e2e_ms / 1e3) / 1e12
+    e2e_value = whole_job_tflops(flops_step, e2e_steps, world, e2e_ms)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
 
