@@ -44,7 +44,7 @@ def _run(eta, B, H, N, d, causal, seed, mask=None, qk_scale=1.0):
     return (q, k, v, do, scale), (dq, dk, dv)
 
 
-def _compare(got, want, label):
+def _compare(got, want, label, fro_tol=1e-2):
     g = got.double().cpu().numpy()
     assert not np.isnan(g).any(), label
     err = np.abs(g - want)
@@ -52,7 +52,7 @@ def _compare(got, want, label):
     assert err.max() <= 2e-2 * ref, (label, float(err.max()), ref)
     nw = float(np.linalg.norm(want))
     fro = float(np.linalg.norm(g - want)) / nw if nw > 1e-6 * math.sqrt(want.size) else 0.0
-    assert fro <= 1e-2, (label, fro)     # (a gradient that is 0 by the definition has no relative error)
+    assert fro <= fro_tol, (label, fro)     # (a gradient that is 0 by the definition has no relative error)
     print(f"{label}: max|err|/max(1,max|ref|) = {float(err.max()) / ref:.3e}, relative Frobenius = {fro:.3e}")
     return float(err.max()) / ref, fro
 
@@ -112,3 +112,25 @@ def test_bwd_rejects_unsupported(eta):
 def test_bwd_full_size_sampled_heads(eta):
     """The bench shape 2x16x4096x128 (non-causal), two heads checked whole."""
     _check(eta, 2, 16, 4096, 128, False, seed=0, heads=[0, 31])
+
+
+def test_bwd_adversarial_logits_causal_masked(eta):
+    """Q and K x30 (scaled scores up to ~5e3), causal, 5% -inf key padding
+    with fully masked rows: the adversarial forward workload's inputs at
+    1 x 4 x 1024 x 128.  Rows are nearly one-hot here, so dS = P (dP - D)
+    is a small difference and the bf16 rounding of O inside D = rowsum(dO*O)
+    shows in dQ and dK: measured relative Frobenius ~9e-3 (2.4e-3 on N(0,1)
+    inputs); the bound for this case is 2e-2."""
+    B, H, N, d = 1, 4, 1024, 128
+    q, k, v = workloads.make_qkv(B, H, N, d, "bf16", 11, qk_scale=30.0)
+    do = workloads.make_grad_out(B, H, N, d, "bf16", 11)
+    mask = workloads.make_key_mask(B, H, N, 0.05, seed=11)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    qc, kc, vc, doc, mc = q.cuda(), k.cuda(), v.cuda(), do.cuda(), mask.cuda()
+    o, lse = eta.attn_fwd(qc, kc, vc, True, scale, key_mask=mc)
+    dq, dk, dv = eta.attn_bwd(qc, kc, vc, o, doc, lse, True, scale, key_mask=mc)
+    assert eta.attn_status() == 0
+    wq, wk, wv = oracle.attn_bwd(q, k, v, do, True, scale, key_mask=mask)
+    for name, got, want in (("dQ", dq, wq), ("dK", dk, wk), ("dV", dv, wv)):
+        _compare(got.cpu(), want, name, fro_tol=2e-2)
+    assert torch.all(dq[0, 0, :4] == 0)      # causal rows 0..3 of head 0 see only masked keys
