@@ -165,27 +165,35 @@ def attn_fwd_block_sparse(q, k, v, block_mask, causal: bool = False, scale: floa
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, Br: int = 0, Bc: int = 0,
-             key_mask=None, out=None, lse=None, stream=None, want_lse: bool = True):
+             key_mask=None, out=None, lse=None, stream=None, want_lse: bool = True, sync: bool = True):
     """Tiled exact attention forward.  Returns (o, lse).
 
     Device tensors: the call is enqueued on `stream` (default: torch's current
     stream) and returns immediately.  Host tensors (pinned or not): inputs are
     copied to the current device, the kernel runs, and o / lse come back as
-    host tensors (end-to-end path).
+    host tensors (end-to-end path), all on `stream`; with sync=False the call
+    returns once that work is enqueued (o / lse are valid after the stream is
+    synchronised), so calls on two streams overlap one's copies with the
+    other's kernel.
     """
     if q.device.type == "cpu":
-        # End-to-end path from host memory, on torch's current stream.
+        # End-to-end path from host memory.
         dev = torch.device("cuda", torch.cuda.current_device())
-        qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
-        md = key_mask.to(dev, non_blocking=True) if key_mask is not None else None
-        o, l = attn_fwd(qd, kd, vd, causal, scale, Br, Bc, md, want_lse=want_lse)
-        ho = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        ho.copy_(o, non_blocking=True)
-        hl = None
-        if l is not None:
-            hl = lse if lse is not None else torch.empty(l.shape, dtype=l.dtype, pin_memory=True)
-            hl.copy_(l, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        st = stream if stream is not None else torch.cuda.current_stream()
+        if not isinstance(st, torch.cuda.Stream):
+            st = torch.cuda.ExternalStream(int(st))
+        with torch.cuda.stream(st):
+            qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
+            md = key_mask.to(dev, non_blocking=True) if key_mask is not None else None
+            o, l = attn_fwd(qd, kd, vd, causal, scale, Br, Bc, md, want_lse=want_lse, stream=st)
+            ho = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+            ho.copy_(o, non_blocking=True)
+            hl = None
+            if l is not None:
+                hl = lse if lse is not None else torch.empty(l.shape, dtype=l.dtype, pin_memory=True)
+                hl.copy_(l, non_blocking=True)
+        if sync:
+            st.synchronize()
         return ho, hl
     for t in (q, k, v):
         if not t.is_cuda or not t.is_contiguous():
