@@ -608,15 +608,29 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             // One loaded 32-column chunk -> log2-domain scores
             // x = s*scale*log2(e) (+ mask*log2(e)), -inf where not allowed.
             auto mask_chunk = [&](int c, uint32_t *r) {
+                if constexpr (MASKED) {
+                    // four staged mask values per broadcast load, two columns per f32x2 FMA
+                    const float4 *m4 = reinterpret_cast<const float4 *>(msm + 32 * c);
+                    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 mv = m4[e4];
+                        float x0, x1, x2, x3;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1])), sl2x2,
+                                         f2_pack(mv.x, mv.y)), x0, x1);
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3])), sl2x2,
+                                         f2_pack(mv.z, mv.w)), x2, x3);
+                        r[4 * e4] = __float_as_uint(x0);
+                        r[4 * e4 + 1] = __float_as_uint(x1);
+                        r[4 * e4 + 2] = __float_as_uint(x2);
+                        r[4 * e4 + 3] = __float_as_uint(x3);
+                    }
+                }
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int key = key0 + 32 * c + e;
-                    float x;
-                    if constexpr (MASKED) {
-                        x = fmaf(__uint_as_float(r[e]), sl2, msm[32 * c + e]);
-                    } else {
-                        x = (key < N) ? __uint_as_float(r[e]) * sl2 : kNegInf;
-                    }
+                    float x = __uint_as_float(r[e]);
+                    if constexpr (!MASKED) x = (key < N) ? x * sl2 : kNegInf;
                     if (diag) x = (key <= row) ? x : kNegInf;
                     if constexpr (BSPARSE) x = dead ? kNegInf : x;
                     r[e] = __float_as_uint(x);
