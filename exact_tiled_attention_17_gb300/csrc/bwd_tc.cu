@@ -540,19 +540,6 @@ __global__ void attn_bwd_finish_kernel(const float4 *__restrict__ acc, uint2 *__
     }
 }
 
-bool make_rows_map(CUtensorMap *m, const void *base, int D, int N, int BH, int box_rows) {
-    EncodeTiledFn enc = encode_tiled_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
-                                static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
-    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // The float32 dQ accumulator [BH][N][D] as a tensor of 32-row boxes (no swizzle).
 bool make_acc_map(CUtensorMap *m, const float *base, int D, int N, int BH) {
     EncodeTiledFn enc = encode_tiled_fn();
@@ -592,9 +579,9 @@ int launch_bwd_d(const void *Q, const void *K, const void *V, const void *O, con
     float *acc = reinterpret_cast<float *>(ws + 2 * round256(static_cast<size_t>(BH) * npad * 4));
 
     CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
-    if (!make_rows_map(&tq, Q, D, N, BH, S::BR) || !make_rows_map(&tk, K, D, N, BH, S::BC) ||
-        !make_rows_map(&tv, V, D, N, BH, S::BC) || !make_rows_map(&tdo, dO, D, N, BH, S::BR) ||
-        !make_rows_map(&tdk, dK, D, N, BH, S::BC) || !make_rows_map(&tdv, dV, D, N, BH, S::BC) ||
+    if (!make_bf16_rows_map(&tq, Q, D, N, BH, S::BR) || !make_bf16_rows_map(&tk, K, D, N, BH, S::BC) ||
+        !make_bf16_rows_map(&tv, V, D, N, BH, S::BC) || !make_bf16_rows_map(&tdo, dO, D, N, BH, S::BR) ||
+        !make_bf16_rows_map(&tdk, dK, D, N, BH, S::BC) || !make_bf16_rows_map(&tdv, dV, D, N, BH, S::BC) ||
         !make_acc_map(&tdq, acc, D, N, BH))
         return kErrCuda;
     int *err = device_error_word();

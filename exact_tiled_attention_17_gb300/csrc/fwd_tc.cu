@@ -1039,19 +1039,6 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
     }
 }
 
-bool make_map(CUtensorMap *m, const void *base, int D, int N, int BH, int box_rows) {
-    EncodeTiledFn enc = encode_tiled_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
-                                static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
-    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int sm_count(int dev) {
     static int counts[64];
     if (dev < 0 || dev >= 64) return 0;
@@ -1085,8 +1072,8 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
         attr_device = dev;
     }
     CUtensorMap tq, tk, tv, to;
-    if (!make_map(&tq, Q, D, N, BH, BR) || !make_map(&tk, K, D, N, BH, BC) || !make_map(&tv, V, D, N, BH, BC) ||
-        !make_map(&to, O, D, N, BH, BR))
+    if (!make_bf16_rows_map(&tq, Q, D, N, BH, BR) || !make_bf16_rows_map(&tk, K, D, N, BH, BC) || !make_bf16_rows_map(&tv, V, D, N, BH, BC) ||
+        !make_bf16_rows_map(&to, O, D, N, BH, BR))
         return kErrCuda;
     TcParams p;
     p.N = N;

@@ -23,6 +23,11 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
 
+// Tensor map of a bf16 [BH][N][D] tensor for 128-byte-swizzled boxes of
+// 64 columns x box_rows rows (the tile layout of the tcgen05 kernels); rows
+// past N read as zero and are dropped on store.
+bool make_bf16_rows_map(CUtensorMap *m, const void *base, int D, int N, int BH, int box_rows);
+
 // Error-word bit set by the emulation kernel for an out-of-range row id
 // (timed-out waits use the low bits).
 constexpr int kErrWordBadRow = 1 << 24;
