@@ -281,15 +281,15 @@ int attn_bwd(const void *Q, const void *K, const void *V, const void *O, const v
     if (causal != 0 && causal != 1) return kErrArg;
     if (dtype != ATTN_BF16) return (dtype == ATTN_F32 || dtype == ATTN_F64) ? kErrUnsupported : kErrArg;
     if (d != 64 && d != 128) return kErrUnsupported;
+    if (!workspace || ws_bytes < attn_bwd_workspace_size(B, H, N, d) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return kErrWorkspace;
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return kErrCuda;
     if (major != 10 || minor != 3) return kErrUnsupported;  // built for sm_103a only
-    if (!workspace || ws_bytes < attn_bwd_workspace_size(B, H, N, d) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return kErrWorkspace;
     rc = launch_bwd_tc_bf16(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, causal, scale, key_mask, workspace,
                             static_cast<cudaStream_t>(stream));
     if (rc == kOk) t_last_variant = d == 64 ? "bwd_tc_bf16_d64_br64_bc128" : "bwd_tc_bf16_d128_br64_bc128";

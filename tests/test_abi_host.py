@@ -126,3 +126,49 @@ def test_debug_timeout_rejects_bad_limit(lib):
     f.argtypes = [ctypes.c_uint, ctypes.c_void_p]
     assert f(0, None) == -1
     assert f(2_000_000, None) == -1
+
+
+def test_backward_and_block_sparse_rejection(lib):
+    vp = ctypes.c_void_p
+    ws_size = lib.attn_bwd_workspace_size
+    ws_size.restype = ctypes.c_size_t
+    ws_size.argtypes = [ctypes.c_int] * 4
+    # LSE and D vectors padded to 64 rows (256-byte aligned each), plus the f32 dQ accumulator
+    assert ws_size(1, 1, 100, 64) == 2 * 512 + 100 * 64 * 4
+    assert ws_size(2, 16, 4096, 128) == 2 * 32 * 4096 * 4 + 32 * 4096 * 128 * 4
+    assert ws_size(0, 1, 100, 64) == 0
+    f = lib.attn_bwd
+    f.restype = ctypes.c_int
+    f.argtypes = [vp] * 9 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]
+    p, big = vp(256), 1 << 30
+
+    def bwd(**kw):
+        a = dict(Q=p, K=p, V=p, O=p, dO=p, LSE=p, dQ=p, dK=p, dV=p, B=1, H=1, N=8, d=64, causal=0, scale=0.125,
+                 dtype=1, mask=None, ws=p, ws_bytes=big)
+        a.update(kw)
+        return f(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["LSE"], a["dQ"], a["dK"], a["dV"], a["B"], a["H"],
+                 a["N"], a["d"], a["causal"], a["scale"], a["dtype"], a["mask"], a["ws"], a["ws_bytes"], None)
+
+    assert bwd(dO=None) == -1
+    assert bwd(LSE=None) == -1
+    assert bwd(dQ=vp(264)) == -1                 # not 16-byte aligned
+    assert bwd(LSE=vp(258)) == -1                # not 4-byte aligned
+    assert bwd(causal=3) == -1
+    assert bwd(dtype=0) == -2                    # float32: bf16 only
+    assert bwd(d=96) == -2
+    assert bwd(ws=None) == -3
+    assert bwd(ws_bytes=100) == -3
+    assert bwd(ws=vp(256 + 16)) == -3            # not 256-byte aligned
+    g = lib.attn_fwd_block_sparse
+    g.restype = ctypes.c_int
+    g.argtypes = [vp] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, vp, vp, vp]
+
+    def bs(**kw):
+        a = dict(N=8, d=64, dtype=1, bm=p)
+        a.update(kw)
+        return g(p, p, p, p, None, 1, 1, a["N"], a["d"], 0, 0.125, a["dtype"], a["bm"], None, None)
+
+    assert bs(bm=None) == -1
+    assert bs(dtype=0) == -2
+    assert bs(d=96) == -2
+    assert bs(N=131073) == -2
