@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 
-SOURCES = ["attn_api.cu", "fwd_tc.cu", "fwd_f32.cu", "naive.cu", "deviation.cu", "emul.cu", "decode.cu", "bwd_tc.cu"]
+SOURCES = ["attn_api.cu", "fwd_tc.cu", "fwd_f32.cu", "naive.cu", "deviation.cu", "emul.cu", "decode.cu", "bwd_tc.cu", "bwd_f32.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "internal.h")] + [os.path.join(INCLUDE, "attn.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -279,7 +279,19 @@ int attn_bwd(const void *Q, const void *K, const void *V, const void *O, const v
     if (!aligned16(dO) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV)) return kErrArg;
     if (reinterpret_cast<uintptr_t>(LSE) & 3u) return kErrArg;
     if (causal != 0 && causal != 1) return kErrArg;
-    if (dtype != ATTN_BF16) return (dtype == ATTN_F32 || dtype == ATTN_F64) ? kErrUnsupported : kErrArg;
+    if (dtype == ATTN_F32) {
+        if (d > 128) return kErrUnsupported;
+        if (!workspace || ws_bytes < attn_bwd_workspace_size(B, H, N, d) ||
+            (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return kErrWorkspace;
+        rc = launch_bwd_f32(static_cast<const float *>(Q), static_cast<const float *>(K), static_cast<const float *>(V),
+                            static_cast<const float *>(O), static_cast<const float *>(dO), LSE, static_cast<float *>(dQ),
+                            static_cast<float *>(dK), static_cast<float *>(dV), B, H, N, d, causal, scale, key_mask,
+                            workspace, static_cast<cudaStream_t>(stream));
+        if (rc == kOk) t_last_variant = "bwd_simt_f32";
+        return rc;
+    }
+    if (dtype != ATTN_BF16) return dtype == ATTN_F64 ? kErrUnsupported : kErrArg;
     if (d != 64 && d != 128) return kErrUnsupported;
     if (!workspace || ws_bytes < attn_bwd_workspace_size(B, H, N, d) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))

@@ -82,6 +82,11 @@ int launch_decode(const void *Q, const void *K, const void *V, void *O, float *L
                   int d, int causal, float scale, int bf16, const float *key_mask, void *workspace,
                   cudaStream_t stream);
 
+// FP32 backward on the CUDA cores (bwd_f32.cu); workspace: B*H*N floats.
+int launch_bwd_f32(const float *Q, const float *K, const float *V, const float *O, const float *dO, const float *LSE,
+                   float *dQ, float *dK, float *dV, int B, int H, int N, int d, int causal, float scale,
+                   const float *key_mask, void *workspace, cudaStream_t stream);
+
 // Backward on tcgen05 (bwd_tc.cu).
 size_t bwd_workspace_bytes(int BH, int N, int d);
 int launch_bwd_tc_bf16(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,

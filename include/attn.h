@@ -216,13 +216,16 @@ int attn_decode_fwd(const void *Q, const void *K, const void *V, void *O, float 
  * [B][H][N][d] bfloat16, written.  All tensor pointers 16-byte aligned,
  * caller-owned device memory.  key_mask: NULL or [B][H][N] additive (finite
  * or -inf), a constant (no gradient is formed for it).  causal as attn_fwd.
- * dtype must be ATTN_BF16 and d 64 or 128, else ATTN_ERR_UNSUPPORTED.
+ * dtype ATTN_BF16 (tensor cores; d 64 or 128) or ATTN_F32 (all tensors
+ * float32, including dQ, dK, dV; CUDA cores, IEEE float32 throughout, no
+ * atomics; d <= 128), else ATTN_ERR_UNSUPPORTED.
  * workspace: at least attn_bwd_workspace_size(B, H, N, d) bytes of device
  * memory, 256-byte aligned (the rows' LSE and D = rowsum(dO * O) vectors and
  * a float32 dQ accumulator), else ATTN_ERR_WORKSPACE.  Asynchronous: three
  * launches on `stream`; errors in the arguments are returned before any
- * launch.  dQ is accumulated with floating-point atomics, so its last bits
- * can differ from run to run; dK and dV are deterministic.
+ * launch.  bf16: dQ is accumulated with floating-point reductions from many
+ * CTAs, so its last bits can differ from run to run; dK and dV are
+ * deterministic.  float32: all three are deterministic.
  */
 size_t attn_bwd_workspace_size(int B, int H, int N, int d);
 int attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,

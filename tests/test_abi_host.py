@@ -154,8 +154,10 @@ def test_backward_and_block_sparse_rejection(lib):
     assert bwd(dQ=vp(264)) == -1                 # not 16-byte aligned
     assert bwd(LSE=vp(258)) == -1                # not 4-byte aligned
     assert bwd(causal=3) == -1
-    assert bwd(dtype=0) == -2                    # float32: bf16 only
-    assert bwd(d=96) == -2
+    assert bwd(dtype=2) == -2                    # float64: bf16 or float32 only
+    assert bwd(dtype=0, d=200) == -2             # float32: d <= 128
+    assert bwd(dtype=0, ws=None) == -3
+    assert bwd(d=96) == -2                       # bf16: d in {64, 128}
     assert bwd(ws=None) == -3
     assert bwd(ws_bytes=100) == -3
     assert bwd(ws=vp(256 + 16)) == -3            # not 256-byte aligned

@@ -96,10 +96,10 @@ def test_bwd_dk_dv_deterministic(eta):
 
 
 def test_bwd_rejects_unsupported(eta):
-    q = torch.zeros((1, 1, 64, 64), dtype=torch.float32, device="cuda")
+    q = torch.zeros((1, 1, 64, 64), dtype=torch.float64, device="cuda")
     lse = torch.zeros((1, 1, 64), dtype=torch.float32, device="cuda")
     with pytest.raises(eta.AttnError):
-        eta.attn_bwd(q, q, q, q, q, lse)                    # float32: bf16 only
+        eta.attn_bwd(q, q, q, q, q, lse)                    # float64: bf16 or float32 only
     qb = torch.zeros((1, 1, 64, 96), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(eta.AttnError):
         eta.attn_bwd(qb, qb, qb, qb, qb, lse)               # d = 96
@@ -134,3 +134,27 @@ def test_bwd_adversarial_logits_causal_masked(eta):
     for name, got, want in (("dQ", dq, wq), ("dK", dk, wk), ("dV", dv, wv)):
         _compare(got.cpu(), want, name, fro_tol=2e-2)
     assert torch.all(dq[0, 0, :4] == 0)      # causal rows 0..3 of head 0 see only masked keys
+
+
+@pytest.mark.parametrize("d", [32, 64, 100, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_f32_matches_oracle(eta, d, causal):
+    """float32 throughout on the CUDA cores: the gradients agree with the FP64
+    chain rule to float32 accuracy (max-abs <= 1e-5 * max(1, max|ref|))."""
+    B, H, N = 1, 3, 333
+    q, k, v = workloads.make_qkv(B, H, N, d, "f32", seed=d)
+    do = workloads.make_grad_out(B, H, N, d, "f32", seed=d)
+    mask = workloads.make_key_mask(B, H, N, 0.1, seed=d)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    qc, kc, vc, doc, mc = q.cuda(), k.cuda(), v.cuda(), do.cuda(), mask.cuda()
+    o, lse = eta.attn_fwd(qc, kc, vc, causal, scale, key_mask=mc)
+    dq, dk, dv = eta.attn_bwd(qc, kc, vc, o, doc, lse, causal, scale, key_mask=mc)
+    assert eta.attn_status() == 0
+    assert eta.attn_last_variant() == "bwd_simt_f32"
+    wq, wk, wv = oracle.attn_bwd(q, k, v, do, causal, scale, key_mask=mask)
+    for name, got, want in (("dQ", dq, wq), ("dK", dk, wk), ("dV", dv, wv)):
+        g = got.double().cpu().numpy()
+        err = float(np.max(np.abs(g - want)))
+        assert err <= 1e-5 * max(1.0, float(np.max(np.abs(want)))), (name, err)
+    if causal:
+        assert torch.all(dq[0, 0, :4] == 0)     # rows whose only keys are masked
