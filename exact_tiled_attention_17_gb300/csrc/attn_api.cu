@@ -124,6 +124,10 @@ int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, i
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
             return kErrCuda;
         if (major != 10 || minor != 3) return kErrUnsupported;  // built for sm_103a only
+        // Default key tile: 128, except short causal d = 64 problems, whose few
+        // tiles per CTA leave the pipeline mostly filling; 64-key tiles with two
+        // S buffers ran 7% faster on 4x16x1024x64 causal.
+        if (Bc == 0 && causal && d == 64 && N <= 1024) Bc = 64;
         rc = launch_fwd_tc_bf16(Q, K, V, O, LSE, B, H, N, d, causal, scale, Br, Bc, key_mask, st, &variant);
     } else if (dtype == ATTN_F32) {
         if (d > 128) return kErrUnsupported;
