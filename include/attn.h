@@ -70,7 +70,8 @@ typedef enum {
  *   probabilities P are rounded to bf16 (round-to-nearest-even) as the
  *   operand of the second contraction and O is rounded to bf16 at the end.
  *   d must be 64 or 128.  Br in {64, 128}, Bc in {64, 128, 256}; 0 selects
- *   128 for either.
+ *   128 for either, except Bc = 0 with causal, d = 64 and N <= 1024, which
+ *   selects 64.
  * dtype ATTN_F32: Q/K/V/O float32, every operation in float32 on the CUDA
  *   cores (no TF32).  1 <= d <= 128.  Br and Bc must be 0 or 64.
  * N >= 1 with any tail; B, H >= 1; B*H*N < 2^31 rows.
