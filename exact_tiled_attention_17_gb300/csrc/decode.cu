@@ -381,9 +381,10 @@ int split_count(int BH, int Nk) {
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) !=
                                                   cudaSuccess)
         nsm = 152;
-    // about two waves of CTAs at three resident per SM, at least 256 keys per
-    // split, at most kDecodeMaxSplits splits
-    int s = (6 * nsm + BH - 1) / BH;
+    // about eight CTAs per SM over the whole grid (more copies in flight: a
+    // sweep of 4, 6, 8 and 12 per SM put 8 ahead on long caches), at least
+    // 256 keys per split, at most kDecodeMaxSplits splits
+    int s = (8 * nsm + BH - 1) / BH;
     const int by_len = (Nk + 255) / 256;
     if (s > by_len) s = by_len;
     if (s > kDecodeMaxSplits) s = kDecodeMaxSplits;
