@@ -26,7 +26,7 @@ round_fmt(x, mbits, ebits)
     Rounding of binary64 values to an IEEE-style format with ``mbits``
     fraction and ``ebits`` exponent bits (round to nearest even, subnormals,
     overflow to infinity), from the definition (``oracle_emul.c``).
-emul(q, k, v, causal, scale, algo, Bc, mbits, ebits, key_mask=None, rows=None)
+emul(q, k, v, causal, scale, algo, Bc, mbits, ebits, key_mask=None, rows=None, plant=0)
     The paper's numerical re-implementation (§III, §IV-A Fig. 3): baseline
     (algo 0) or tiled (algo 1, key blocks of width Bc) attention with every
     tensor operation's result rounded to that format (``oracle_emul.c``).
@@ -97,6 +97,8 @@ def _load():
                                              ctypes.c_int, ctypes.c_int, lp, ctypes.c_longlong, dp,
                                              ctypes.c_int]
             lib.oracle_emul_rows.restype = ctypes.c_int
+            lib.oracle_emul_rows_planted.argtypes = lib.oracle_emul_rows.argtypes + [ctypes.c_int]
+            lib.oracle_emul_rows_planted.restype = ctypes.c_int
             lib.oracle_attn_bwd_f64.argtypes = [dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, ctypes.c_double, lp, ctypes.c_longlong,
                                                 dp, dp, dp, ctypes.c_int, ctypes.c_int]
@@ -226,12 +228,23 @@ def round_fmt(x, mbits: int, ebits: int) -> np.ndarray:
     return Y
 
 
+# Planted mistakes of the emulation (oracle_emul.c), for the oracle's own tests:
+# each names the rounding site that is left out, moved or duplicated.
+EMUL_PLANTS = {
+    "q_in": 1, "k_in": 2, "v_in": 3, "score": 4, "mask_add": 5, "m_diff": 6, "a_exp": 7, "s_diff": 8,
+    "p_exp": 9, "a_times_l": 10, "rowsum": 11, "l_add": 12, "a_times_o": 13, "pv": 14, "o_add": 15,
+    "div": 16, "l_late": 17, "pv_per_key": 18, "dot_per_term": 19, "softmax": 20, "base_pv": 21,
+    "softmax_ops": 22,
+}
+
+
 def emul(q, k, v, causal: bool, scale: float, algo: int, Bc: int, mbits: int, ebits: int,
-         key_mask=None, rows=None, nthreads: int | None = None) -> np.ndarray:
+         key_mask=None, rows=None, nthreads: int | None = None, plant: int = 0) -> np.ndarray:
     """Attention with every tensor op rounded to a format (see oracle_emul.c).
 
     algo 0: baseline (softmax, then P V); algo 1: tiled online merge over key
     blocks of width Bc.  Returns O [..., N, d] for all rows, or [nrows, d].
+    ``plant`` (a value of EMUL_PLANTS) is for the oracle's own tests.
     """
     lib = _load()
     Q, K, V = _f64(q), _f64(k), _f64(v)
@@ -248,10 +261,10 @@ def emul(q, k, v, causal: bool, scale: float, algo: int, Bc: int, mbits: int, eb
     R = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     nrows = BH * N if R is None else R.size
     O = np.zeros((nrows, d), dtype=np.float64)
-    rc = lib.oracle_emul_rows(_ptr(Q), _ptr(K), _ptr(V), _ptr(M) if M is not None else None, BH, N, d,
-                              1 if causal else 0, float(scale), int(algo), int(Bc), int(mbits), int(ebits),
-                              _ptr(R, ctypes.c_longlong) if R is not None else None, nrows, _ptr(O),
-                              nthreads or default_threads())
+    rc = lib.oracle_emul_rows_planted(_ptr(Q), _ptr(K), _ptr(V), _ptr(M) if M is not None else None, BH, N, d,
+                                      1 if causal else 0, float(scale), int(algo), int(Bc), int(mbits),
+                                      int(ebits), _ptr(R, ctypes.c_longlong) if R is not None else None, nrows,
+                                      _ptr(O), nthreads or default_threads(), int(plant))
     if rc != 0:
         raise RuntimeError("oracle_emul_rows failed")
     return O.reshape(*lead, N, d) if R is None else O

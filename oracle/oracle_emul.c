@@ -43,10 +43,44 @@
  *             and at the end o = fl(o / l) (0 for a row with no allowed key).
  *    With F = binary64 both algorithms give softmax(QK^T*scale + mask)V up to
  *    binary64 rounding, which the tests check against oracle_attn_rows_f64.
+ *
+ *  oracle_emul_rows_planted — the same with one planted mistake, for the
+ *    oracle's own tests only: `plant` names one rounding site above whose
+ *    fl() is left out (or, for the last few, moved or duplicated).  The
+ *    tests show that hand-worked rows in a coarse format tell every planted
+ *    variant from the one above.  plant = 0 is oracle_emul_rows.
  */
 #include <math.h>
 #include <pthread.h>
 #include <stdlib.h>
+
+/* planted mistakes (test infrastructure): the rounding site that is changed */
+enum {
+    PLANT_NONE = 0,
+    PLANT_Q_IN = 1,       /* Q used without rounding to F */
+    PLANT_K_IN = 2,       /* K used without rounding to F */
+    PLANT_V_IN = 3,       /* V used without rounding to F */
+    PLANT_SCORE = 4,      /* scale * (q . k) not rounded */
+    PLANT_MASK_ADD = 5,   /* s + mask not rounded */
+    PLANT_M_DIFF = 6,     /* m - M' not rounded */
+    PLANT_A_EXP = 7,      /* exp(m - M') not rounded */
+    PLANT_S_DIFF = 8,     /* s_j - M' not rounded */
+    PLANT_P_EXP = 9,      /* exp(s_j - M') not rounded */
+    PLANT_AL = 10,        /* a * l not rounded */
+    PLANT_ROWSUM = 11,    /* sum_j p_j of a block not rounded */
+    PLANT_L_ADD = 12,     /* the sum a*l + rowsum not rounded */
+    PLANT_AO = 13,        /* a * o not rounded */
+    PLANT_PV = 14,        /* a block's P V not rounded */
+    PLANT_O_ADD = 15,     /* the sum a*o + P V not rounded */
+    PLANT_DIV = 16,       /* the final o / l not rounded */
+    PLANT_L_LATE = 17,    /* l kept in binary64 and rounded once, at the end */
+    PLANT_PV_PER_KEY = 18,/* P V rounded after every key instead of once per block */
+    PLANT_DOT_PER_TERM = 19, /* q . k rounded after every term (a duplicated fl) */
+    PLANT_SOFTMAX = 20,   /* baseline: P = softmax(s) not rounded */
+    PLANT_BASE_PV = 21,   /* baseline: P V not rounded */
+    PLANT_SOFTMAX_OPS = 22, /* baseline: exp, sum and division each rounded (three ops, not one) */
+    PLANT_LAST = 22
+};
 
 double oracle_round_fmt(double x, int mbits, int ebits)
 {
@@ -72,7 +106,7 @@ void oracle_round_array(const double *x, double *y, long long n, int mbits, int 
 
 typedef struct {
     const double *Q, *K, *V, *mask;
-    int N, d, causal, algo, Bc, mbits, ebits;
+    int N, d, causal, algo, Bc, mbits, ebits, plant;
     double scale;
     const long long *rows;
     long long nrows;
@@ -83,6 +117,8 @@ typedef struct {
 } emul_job_t;
 
 #define FL(v) oracle_round_fmt((v), job->mbits, job->ebits)
+/* fl() at a named site: left out when that site is the planted one */
+#define FLS(site, v) (job->plant == (site) ? (v) : FL(v))
 
 /* scores of one query row, rounded as described above */
 static void emul_scores(const emul_job_t *job, long long bh, int i, double *s)
@@ -96,11 +132,14 @@ static void emul_scores(const emul_job_t *job, long long bh, int i, double *s)
         }
         const double *k = job->K + (bh * N + j) * (long long)d;
         double dot = 0.0;
-        for (int c = 0; c < d; ++c) dot += FL(q[c]) * FL(k[c]);
-        double x = FL(job->scale * dot);
+        for (int c = 0; c < d; ++c) {
+            dot += FLS(PLANT_Q_IN, q[c]) * FLS(PLANT_K_IN, k[c]);
+            if (job->plant == PLANT_DOT_PER_TERM) dot = FL(dot);
+        }
+        double x = FLS(PLANT_SCORE, job->scale * dot);
         if (job->mask) {
             const double mk = job->mask[bh * N + j];
-            x = isinf(mk) && mk < 0 ? -INFINITY : FL(x + mk);
+            x = isinf(mk) && mk < 0 ? -INFINITY : FLS(PLANT_MASK_ADD, x + mk);
         }
         s[j] = x;
     }
@@ -121,16 +160,18 @@ static void emul_row(const emul_job_t *job, long long flat, double *s, double *p
             for (int c = 0; c < d; ++c) o[c] = 0.0;
             return;
         }
+        const int ops = job->plant == PLANT_SOFTMAX_OPS;
         double sum = 0.0;
         for (int j = 0; j < N; ++j) {
-            p[j] = exp(s[j] - mx);
+            p[j] = ops ? FL(exp(FL(s[j] - mx))) : exp(s[j] - mx);
             sum += p[j];
         }
-        for (int j = 0; j < N; ++j) p[j] = FL(p[j] / sum);
+        if (ops) sum = FL(sum);
+        for (int j = 0; j < N; ++j) p[j] = FLS(PLANT_SOFTMAX, p[j] / sum);
         for (int c = 0; c < d; ++c) {
             double acc = 0.0;
-            for (int j = 0; j < N; ++j) acc += p[j] * FL(V[(long long)j * d + c]);
-            o[c] = FL(acc);
+            for (int j = 0; j < N; ++j) acc += p[j] * FLS(PLANT_V_IN, V[(long long)j * d + c]);
+            o[c] = FLS(PLANT_BASE_PV, acc);
         }
         return;
     }
@@ -143,21 +184,28 @@ static void emul_row(const emul_job_t *job, long long flat, double *s, double *p
         for (int j = j0; j < j1; ++j) mb = s[j] > mb ? s[j] : mb;
         const double M = m > mb ? m : mb;
         const double Mu = (M == -INFINITY) ? 0.0 : M;
-        const double a = (m == -INFINITY) ? 0.0 : FL(exp(FL(m - Mu)));
+        const double a = (m == -INFINITY) ? 0.0 : FLS(PLANT_A_EXP, exp(FLS(PLANT_M_DIFF, m - Mu)));
         double rs = 0.0;
         for (int j = j0; j < j1; ++j) {
-            p[j] = (s[j] == -INFINITY) ? 0.0 : FL(exp(FL(s[j] - Mu)));
+            p[j] = (s[j] == -INFINITY) ? 0.0 : FLS(PLANT_P_EXP, exp(FLS(PLANT_S_DIFF, s[j] - Mu)));
             rs += p[j];
         }
-        l = FL(FL(a * l) + FL(rs));
+        if (job->plant == PLANT_L_LATE)
+            l = a * l + rs;
+        else
+            l = FLS(PLANT_L_ADD, FLS(PLANT_AL, a * l) + FLS(PLANT_ROWSUM, rs));
         for (int c = 0; c < d; ++c) {
             double acc = 0.0;
-            for (int j = j0; j < j1; ++j) acc += p[j] * FL(V[(long long)j * d + c]);
-            o[c] = FL(FL(a * o[c]) + FL(acc));
+            for (int j = j0; j < j1; ++j) {
+                acc += p[j] * FLS(PLANT_V_IN, V[(long long)j * d + c]);
+                if (job->plant == PLANT_PV_PER_KEY) acc = FL(acc);
+            }
+            o[c] = FLS(PLANT_O_ADD, FLS(PLANT_AO, a * o[c]) + FLS(PLANT_PV, acc));
         }
         m = M;
     }
-    for (int c = 0; c < d; ++c) o[c] = (l == 0.0) ? 0.0 : FL(o[c] / l);
+    if (job->plant == PLANT_L_LATE) l = FL(l);
+    for (int c = 0; c < d; ++c) o[c] = (l == 0.0) ? 0.0 : FLS(PLANT_DIV, o[c] / l);
 }
 
 static void *emul_worker(void *arg)
@@ -186,12 +234,12 @@ static void *emul_worker(void *arg)
     return NULL;
 }
 
-int oracle_emul_rows(const double *Q, const double *K, const double *V, const double *mask, int BH, int N,
-                     int d, int causal, double scale, int algo, int Bc, int mbits, int ebits,
-                     const long long *rows, long long nrows, double *O, int nthreads)
+int oracle_emul_rows_planted(const double *Q, const double *K, const double *V, const double *mask, int BH,
+                             int N, int d, int causal, double scale, int algo, int Bc, int mbits, int ebits,
+                             const long long *rows, long long nrows, double *O, int nthreads, int plant)
 {
     if (!Q || !K || !V || !O || BH <= 0 || N <= 0 || d <= 0 || Bc <= 0 || mbits < 1 || mbits > 52 ||
-        ebits < 2 || ebits > 11 || (algo != 0 && algo != 1))
+        ebits < 2 || ebits > 11 || (algo != 0 && algo != 1) || plant < 0 || plant > PLANT_LAST)
         return -1;
     if (rows)
         for (long long r = 0; r < nrows; ++r)
@@ -208,6 +256,7 @@ int oracle_emul_rows(const double *Q, const double *K, const double *V, const do
     job.Bc = Bc;
     job.mbits = mbits;
     job.ebits = ebits;
+    job.plant = plant;
     job.scale = scale;
     job.rows = rows;
     job.nrows = rows ? nrows : (long long)BH * N;
@@ -227,4 +276,12 @@ int oracle_emul_rows(const double *Q, const double *K, const double *V, const do
     for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
     pthread_mutex_destroy(&job.lock);
     return job.fail ? -1 : 0;
+}
+
+int oracle_emul_rows(const double *Q, const double *K, const double *V, const double *mask, int BH, int N,
+                     int d, int causal, double scale, int algo, int Bc, int mbits, int ebits,
+                     const long long *rows, long long nrows, double *O, int nthreads)
+{
+    return oracle_emul_rows_planted(Q, K, V, mask, BH, N, d, causal, scale, algo, Bc, mbits, ebits, rows, nrows, O,
+                                    nthreads, PLANT_NONE);
 }

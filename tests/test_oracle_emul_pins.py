@@ -10,7 +10,11 @@ things it does not compute itself:
 - at binary64 both emulated algorithms against the direct FP64 definition of
   attention (``oracle.attn``), for every key-block width;
 - the trend the paper reports in Fig. 3: the FlashAttention-vs-baseline
-  deviation shrinks as the format's fraction bits grow.
+  deviation shrinks as the format's fraction bits grow;
+- below binary64, rows worked by hand in a coarse format (2 fraction bits,
+  5 exponent bits; ``tests/golden/emul_e5m2_rows.json``), which every
+  planted mistake in the oracle's rounding (a left-out, moved or duplicated
+  fl()) fails.
 """
 import math
 
@@ -130,3 +134,60 @@ def test_emul_row_subset_matches_full():
     rows = np.array([0, 5, 39, 40, 119])
     sub = oracle.emul(q, k, v, True, 0.3, 1, 8, 7, 8, rows=rows)
     assert np.array_equal(sub, full[rows])
+
+
+def test_round_e5m2_matches_torch_float8_conversion():
+    """The coarse format of the hand-worked rows below (2 fraction bits, 5
+    exponent bits) is the E5M2 layout, which torch converts to with round to
+    nearest even, subnormals and overflow to infinity."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e5m2"):
+        pytest.skip("torch has no float8_e5m2")
+    rng = np.random.default_rng(12)
+    x32 = _wide_values(rng, 20000, -18, 17).astype(np.float32)   # subnormal E5M2 .. overflow
+    want = torch.from_numpy(x32).to(torch.float8_e5m2).to(torch.float64).numpy()
+    got = oracle.round_fmt(x32.astype(np.float64), 2, 5)
+    assert np.array_equal(got, want)
+
+
+def _golden_rows(golden_dir):
+    import json
+    import os
+    with open(os.path.join(golden_dir, "emul_e5m2_rows.json")) as f:
+        g = json.load(f)
+    return g["format"]["mbits"], g["format"]["ebits"], g["cases"]
+
+
+def _run_golden_row(case, mbits, ebits, plant=0):
+    N = len(case["k"])
+    q = np.full((1, N, 1), float(case["q"]))
+    k = np.asarray(case["k"], dtype=np.float64).reshape(1, N, 1)
+    v = np.asarray(case["v"], dtype=np.float64).reshape(1, N, 1)
+    mask = None if case["mask"] is None else np.asarray(case["mask"], dtype=np.float64).reshape(1, N)
+    out = oracle.emul(q, k, v, False, case["scale"], case["algo"], case["Bc"], mbits, ebits, key_mask=mask,
+                      rows=[N - 1], plant=plant)
+    return float(out[0, 0])
+
+
+def test_emul_hand_worked_rows_e5m2(golden_dir):
+    """Rows worked by hand, step by step, in the E5M2 layout (tests/golden/emul_e5m2_rows.json):
+    both algorithms of the instrument, key blocks of 1 and 2, finite key masks.
+    The oracle must give exactly the hand-worked output."""
+    mb, eb, cases = _golden_rows(golden_dir)
+    for case in cases:
+        assert _run_golden_row(case, mb, eb) == case["O"], case["name"]
+
+
+@pytest.mark.parametrize("site", sorted(oracle.EMUL_PLANTS))
+def test_emul_planted_mistakes_fail_hand_worked_rows(golden_dir, site):
+    """Every rounding site of the instrument is pinned: leaving one fl() out
+    (Q, K or V not rounded first; the score, the mask sum, m - M, either exp,
+    a*l, the row sum, the l update, a*o, the block's P V, the o update, the
+    final division; the baseline's softmax or P V), rounding l only at the
+    end, rounding P V after every key, rounding q.k after every term, or
+    splitting the baseline softmax into three rounded ops changes the output
+    of at least one hand-worked row."""
+    mb, eb, cases = _golden_rows(golden_dir)
+    plant = oracle.EMUL_PLANTS[site]
+    changed = [c["name"] for c in cases if _run_golden_row(c, mb, eb, plant) != c["O"]]
+    assert changed, f"planted mistake '{site}' is not caught by any hand-worked row"
