@@ -245,18 +245,27 @@ def attn_deviation_workspace_size(n: int) -> int:
     return int(lib.attn_deviation_workspace_size(int(n)))
 
 
-def attn_deviation(a, b, workspace=None, stream=None) -> dict:
-    """Deviation between two device tensors of equal size (synchronous)."""
+def _same_device(a, b):
     if a.numel() != b.numel():
         raise ValueError("a and b must have the same number of elements")
+    if not (a.is_cuda and b.is_cuda) or a.device != b.device:
+        raise ValueError("a and b must be tensors on one CUDA device")
+
+
+def attn_deviation(a, b, workspace=None, stream=None) -> dict:
+    """Deviation between two device tensors of equal size (synchronous)."""
+    _same_device(a, b)
     a = a.contiguous()
     b = b.contiguous()
     n = a.numel()
-    ws = workspace if workspace is not None else torch.empty(attn_deviation_workspace_size(n), dtype=torch.uint8,
-                                                             device=a.device)
-    res = DevT()
-    rc = lib.attn_deviation(_ptr(a), _DTYPE[a.dtype], _ptr(b), _DTYPE[b.dtype], n, _ptr(ws), ws.numel(),
-                            ctypes.c_void_p(_stream(stream)), ctypes.byref(res))
+    with torch.cuda.device(a.device):   # the library launches on the current device
+        ws = workspace if workspace is not None else torch.empty(attn_deviation_workspace_size(n),
+                                                                 dtype=torch.uint8, device=a.device)
+        if not ws.is_cuda or ws.device != a.device:
+            raise ValueError("workspace must be on the tensors' device")
+        res = DevT()
+        rc = lib.attn_deviation(_ptr(a), _DTYPE[a.dtype], _ptr(b), _DTYPE[b.dtype], n, _ptr(ws), ws.numel(),
+                                ctypes.c_void_p(_stream(stream)), ctypes.byref(res))
     _check(rc, "attn_deviation")
     return {"max_abs": res.max_abs, "w1": res.w1, "mean_abs": res.mean_abs, "std_abs": res.std_abs,
             "mean_signed": res.mean_signed, "n": res.n}
@@ -266,13 +275,13 @@ def attn_deviation_noalloc(a, b, stream=None) -> dict:
     """attn_deviation without a workspace, for callers that cannot allocate
     device memory (the library's own fixed scratch array is used instead;
     n <= DEVIATION_NOALLOC_MAX_N; calls that overlap on the GPU race)."""
-    if a.numel() != b.numel():
-        raise ValueError("a and b must have the same number of elements")
+    _same_device(a, b)
     a = a.contiguous()
     b = b.contiguous()
     res = DevT()
-    rc = lib.attn_deviation_noalloc(_ptr(a), _DTYPE[a.dtype], _ptr(b), _DTYPE[b.dtype], a.numel(),
-                                    ctypes.c_void_p(_stream(stream)), ctypes.byref(res))
+    with torch.cuda.device(a.device):   # the scratch array and the launch follow the current device
+        rc = lib.attn_deviation_noalloc(_ptr(a), _DTYPE[a.dtype], _ptr(b), _DTYPE[b.dtype], a.numel(),
+                                        ctypes.c_void_p(_stream(stream)), ctypes.byref(res))
     _check(rc, "attn_deviation_noalloc")
     return {"max_abs": res.max_abs, "w1": res.w1, "mean_abs": res.mean_abs, "std_abs": res.std_abs,
             "mean_signed": res.mean_signed, "n": res.n}

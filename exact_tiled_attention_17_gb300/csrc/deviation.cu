@@ -348,7 +348,8 @@ static __device__ __align__(256) unsigned char g_deviation_scratch[kNoAllocBytes
 
 namespace {
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[64];   // device address of g_deviation_scratch, per device
+void *g_scratch_ptr[64];   // device address of g_deviation_scratch, per device (stale after a
+                           // cudaDeviceReset of that device: the header says not to call then)
 }  // namespace
 
 int launch_deviation_noalloc(const void *a, int ta, const void *b, int tb, long long n, cudaStream_t stream,

@@ -130,8 +130,7 @@ struct TcShape {
     static constexpr int BAR_PVDONE = BAR_OFULL + NQ;   // two S buffers: each P_q V has completed
     static constexpr int BAR_DONE = BAR_PVDONE + NQ;
     static constexpr int BAR_PART = BAR_DONE + 1;       // split K/V: partials of the other parts are ready
-    static constexpr int BAR_DONEREAD = BAR_PART + 1;   // split K/V: the first part has read this one's partial
-    static constexpr int NBARS = BAR_DONEREAD + 1;
+    static constexpr int NBARS = BAR_PART + 1;
     // split K/V: a part's partial results, staged in the (then idle) Q tiles and K/V ring:
     // unnormalised O rows (float32, padded stride) and the per-row m, l
     static constexpr int PSTR = D + 4;
@@ -246,7 +245,6 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         }
         mbar_init(bar(S::BAR_DONE), 1);
         mbar_init(bar(S::BAR_PART), static_cast<uint32_t>((nparts > 1 ? nparts - 1 : 1) * S::SOFTMAX_WARPS * 32));
-        mbar_init(bar(S::BAR_DONEREAD), 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -923,18 +921,25 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                     asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(1)), "f"(l) : "memory");
                 }
                 mbar_arrive_remote(mapa_shared(bar(S::BAR_PART), 0));
-                // this CTA's shared memory must outlive the first part's reads
-                mbar_wait_cluster(bar(S::BAR_DONEREAD), 0, abort_flag, p.err, 22);
+                // This CTA's shared memory outlives the first part's reads: every
+                // thread of every part meets at the cluster barrier at the end.
                 write_out = false;
             } else if (nparts > 1) {
-                mbar_wait_cluster(bar(S::BAR_PART), 0, abort_flag, p.err, 23);
+                // A failed wait (the error word has it) reads no partial: the
+                // merge then has only this part's keys, and the O / LSE stores
+                // below are skipped because the abort flag is set.
+                const bool parts_ok = mbar_wait_cluster(bar(S::BAR_PART), 0, abort_flag, p.err, 23);
                 float mp[8], lp[8];
                 m_fin = m;
 #pragma unroll
                 for (int pp = 1; pp < 8; ++pp) {
                     if (pp >= nparts) break;
-                    mp[pp] = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
-                    lp[pp] = ld_cluster_f32(mapa_shared(stat_addr(1), pp));
+                    mp[pp] = kNegInf;
+                    lp[pp] = 0.f;
+                    if (parts_ok) {
+                        mp[pp] = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
+                        lp[pp] = ld_cluster_f32(mapa_shared(stat_addr(1), pp));
+                    }
                     m_fin = fmaxf(m_fin, mp[pp]);
                 }
                 if (m_fin == kNegInf) {
@@ -1016,17 +1021,8 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                 tma_store_commit();
                 tma_store_wait_read0();
             }
-            if (h == 0 && active && p.lse != nullptr && row < N) {
+            if (h == 0 && active && p.lse != nullptr && row < N && !*abort_flag) {
                 p.lse[static_cast<size_t>(bh) * N + row] = any ? (m_fin + log2f(l_fin)) * kLn2 : kNegInf;
-            }
-        }
-        if constexpr (S::CAN_SPLIT) {
-            if (nparts > 1 && part == 0) {
-                // every softmax thread of the first part has read the other
-                // parts' shared memory: they may exit
-                named_bar_sync(9, S::SOFTMAX_WARPS * 32);
-                if (threadIdx.x == 0)
-                    for (int pp = 1; pp < nparts; ++pp) mbar_arrive_remote(mapa_shared(bar(S::BAR_DONEREAD), pp));
             }
         }
     }
@@ -1036,6 +1032,12 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
     if (warp == S::WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, S::TMEM_COLS);
+    }
+    if constexpr (S::CAN_SPLIT) {
+        // Split item: no part exits while the first part may still read its
+        // shared memory.  Every thread reaches this point on every path (all
+        // waits above are bounded), so the barrier always completes.
+        if (nparts > 1) cluster_sync();
     }
 }
 

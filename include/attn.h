@@ -169,7 +169,10 @@ int attn_deviation(const void *a, int ta, const void *b, int tb, long long n,
  * Larger n returns ATTN_ERR_UNSUPPORTED (use attn_deviation with a workspace).
  * It calls no cudaMalloc or cudaFree.  The first call on a device looks up
  * the array's device address on that device; make that first call before
- * any stream capture begins.  All calls share the one array, so calls that
+ * any stream capture begins.  That address is kept for the life of the
+ * process: after a cudaDeviceReset of a device it is stale (the runtime loads
+ * the array again elsewhere), so do not call this entry point on a device
+ * that has been reset.  All calls share the one array, so calls that
  * can overlap on the GPU (different streams or threads at the same time)
  * race with each other and must be serialised by the caller.  Arguments and
  * result as for attn_deviation; synchronous.

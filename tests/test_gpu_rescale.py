@@ -1,0 +1,165 @@
+"""GPU parity of the tensor-core forward where its rescaling shortcuts decide.
+
+The kernel keeps each row's online-softmax state as the yadro-code.ru
+FlashAttention tutorial describes it (a running maximum, a running
+denominator and an unnormalised accumulator, brought to a common maximum
+when a block with a larger one arrives), with two shortcuts that are exact up
+to rounding because O / l does not depend on the reference point:
+
+- key tiles of 64 or 128 columns: the reference maximum is the first tile's;
+  a later tile is exponentiated against it and redone against the row's new
+  maximum only if the p sum over one warpgroup's columns passes 2^16;
+- key tiles of 256 columns: the reference moves only when a tile's maximum
+  exceeds it by more than 8 (log2 units).
+
+These tests put row scores just below and just above both limits, on every
+(d, Br, Bc) variant, causal and not, through exact embeddings (q = e0 plus a
+small second component, k_j = s_j e0 plus a small second component, scale =
+ln 2 so that a score is its own log2-domain value).  They also run the
+adversarial workload's generator (Q and K x30, -inf key padding, fully
+masked rows) through every variant and through the K/V-split cluster tail.
+Bar: the forward's bf16 tolerance against the FP64 oracle (O max-abs 2e-2;
+LSE 1e-3 + 2e-6 |LSE|; fully masked rows O = 0, LSE = -inf).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity import run_case
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [(d, br, bc) for d in (64, 128) for br in (64, 128) for bc in (64, 128, 256)]
+SCALE = float(np.float32(math.log(2.0)))   # score s * scale * log2(e) = s (to float32 rounding)
+
+
+@pytest.fixture(scope="module")
+def eta():
+    import exact_tiled_attention_17_gb300 as m
+    return m
+
+
+def _embedding(N, d, Bc, high, low, H=2, seed=0):
+    """q_i = e0 + c_i e1, k_j = x_j e0 + r_j e1 (bf16-exact), V ~ N(0, 1).
+
+    Key tile t = keys [t*Bc, (t+1)*Bc): one key (its column moves from tile to
+    tile) at score high(t), the others at low(t).  c_i in {-1, 0, 1}, r_j in
+    {-0.25, 0, 0.25}, so a row's scores differ from x_j by at most 0.25."""
+    x = np.empty(N)
+    for t in range(-(-N // Bc)):
+        j0, j1 = t * Bc, min(N, (t + 1) * Bc)
+        x[j0:j1] = low(t)
+        hk = j0 + (37 * t + 5) % Bc
+        if hk < j1:
+            x[hk] = high(t)
+    q = torch.zeros(1, H, N, d)
+    k = torch.zeros(1, H, N, d)
+    q[..., 0] = 1.0
+    q[..., 1] = torch.tensor([(i % 3) - 1.0 for i in range(N)])
+    k[..., 0] = torch.from_numpy(x).float()
+    k[..., 1] = torch.tensor([0.25 * ((j % 3) - 1) for j in range(N)])
+    qb, kb = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    assert torch.equal(qb.float(), q) and torch.equal(kb.float(), k), "embedding must be bf16-exact"
+    g = torch.Generator().manual_seed(seed)
+    v = torch.randn(1, H, N, d, generator=g).to(torch.bfloat16)
+    return qb, kb, v
+
+
+# plateau: the first tile's keys at 0 set the reference; every later tile has
+# one key at `delta` above it and the rest at 0.
+#   delta 15.5: a tile's sum stays below 2^16 (no redo); 16.5: above (redo).
+#   delta 7 / 9: below / above the 256-column variant's move limit of 8.
+@pytest.mark.parametrize("delta", [7.0, 9.0, 15.5, 16.5])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d,Br,Bc", VARIANTS)
+def test_reference_plateau_around_limits(eta, d, Br, Bc, causal, delta):
+    N = 1000
+    qkv = _embedding(N, d, Bc, high=lambda t: 0.0 if t == 0 else delta, low=lambda t: 0.0, seed=int(delta))
+    run_case(eta, 1, 2, N, d, "bf16", causal, Br=Br, Bc=Bc, scale=SCALE, qkv=qkv)
+    assert f"_br{Br}_bc{Bc}_" in eta.attn_last_variant()
+
+
+# staircase: tile t's high key at delta * (t mod 8), the rest 20 below it.
+#   delta 17: every step passes 2^16 (a redo per tile); delta 15: every other
+#   step does (the reference moves on alternate tiles).
+@pytest.mark.parametrize("delta", [15.0, 17.0])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d,Br,Bc", VARIANTS)
+def test_reference_staircase(eta, d, Br, Bc, causal, delta):
+    N = 1000
+    qkv = _embedding(N, d, Bc, high=lambda t: delta * (t % 8), low=lambda t: delta * (t % 8) - 20.0,
+                     seed=int(delta) + 1)
+    run_case(eta, 1, 2, N, d, "bf16", causal, Br=Br, Bc=Bc, scale=SCALE, qkv=qkv)
+
+
+def _adversarial(B, H, N, d, seed, all_masked_head=None):
+    q, k, v = workloads.make_qkv(B, H, N, d, "bf16", seed, qk_scale=30.0)
+    mask = workloads.make_key_mask(B, H, N, 0.05, seed=seed)
+    if all_masked_head is not None:
+        mask[0, all_masked_head, :] = float("-inf")
+    return q, k, v, mask
+
+
+def _fully_masked_rows(mask, causal):
+    m = mask.numpy().reshape(-1, mask.shape[-1])
+    out = []
+    for bh in range(m.shape[0]):
+        allowed = np.cumsum(np.isfinite(m[bh])) if causal else np.full(m.shape[1], np.isfinite(m[bh]).sum())
+        out += [bh * m.shape[1] + i for i in np.nonzero(allowed == 0)[0]]
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d,Br,Bc", VARIANTS)
+def test_adversarial_logits_every_variant(eta, d, Br, Bc, causal):
+    """The adversarial workload's generator at 1 x 4 x 1000: Q, K x30 (scaled
+    scores in the thousands), 5% -inf key padding, keys 0..3 masked in head
+    0 (causal rows 0..3 fully masked) and head 1 masked whole."""
+    B, H, N = 1, 4, 1000
+    q, k, v, mask = _adversarial(B, H, N, d, seed=d + Br + Bc, all_masked_head=1)
+    assert len(_fully_masked_rows(mask, causal)) > 0
+    run_case(eta, B, H, N, d, "bf16", causal, Br=Br, Bc=Bc, mask=mask, qkv=(q, k, v))
+    assert f"_br{Br}_bc{Bc}_" in eta.attn_last_variant()
+
+
+def _heads_for_split(nsm, num_qg, split, nkv):
+    """Heads H (B = 1) whose launch ends in a tail wave that the launcher splits
+    into `split` parts: items = H * num_qg = k * nsm + R with split * R <= nsm
+    and (for split < 8) 2 * split * R > nsm."""
+    if nsm % split or split > nkv:
+        return None
+    for R in range(1, nsm + 1):
+        if split * R > nsm:
+            break
+        if split < 8 and 2 * split * R <= nsm:
+            continue
+        if (nsm + R) % num_qg == 0:
+            return (nsm + R) // num_qg
+    return None
+
+
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("d,Bc", [(128, 128), (64, 128), (128, 64), (64, 256)])
+def test_adversarial_logits_split_tail(eta, d, Bc, split):
+    """Non-causal items past the last full wave are split along K/V over the
+    CTAs of a cluster and merged with the tiles' rescale rule.  Heads are
+    chosen from the SM count so that the tail splits into 2, 4 or 8 parts;
+    one head has every key masked (each part's maximum is -inf)."""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    N, Br = 1000, 128
+    nq = 2 if 2 * (Bc + d) <= 512 else 1
+    num_qg = -(-N // (nq * Br))
+    H = _heads_for_split(nsm, num_qg, split, -(-N // Bc))
+    if H is None:
+        pytest.skip(f"no head count splits the tail {split} ways on {nsm} SMs with Bc={Bc}")
+    q, k, v, mask = _adversarial(1, H, N, d, seed=split + d, all_masked_head=2)
+    extra = _fully_masked_rows(mask, False)
+    rows = workloads.sample_rows(1, H, N, 1 / 16, seed=split, extra=extra)
+    run_case(eta, 1, H, N, d, "bf16", False, Br=Br, Bc=Bc, mask=mask, rows=rows, qkv=(q, k, v))
+    assert f"_kvsplit{split}" in eta.attn_last_variant()
+    # the same heads unmasked, N(0, 1) inputs
+    run_case(eta, 1, H, N, d, "bf16", False, Br=Br, Bc=Bc, rows=rows, seed=split)
+    assert f"_kvsplit{split}" in eta.attn_last_variant()
