@@ -31,7 +31,7 @@ ATTN_ERR_CUDA = -4
 ATTN_ERR_DEVICE_TIMEOUT = -5
 
 # Every symbol include/attn.h declares.
-EXPORTS = ("attn_fwd", "attn_fwd_block_sparse", "attn_naive_workspace_size", "attn_naive_fwd", "attn_deviation_workspace_size",
+EXPORTS = ("attn_fwd", "attn_fwd_host_workspace_size", "attn_fwd_host", "attn_fwd_block_sparse", "attn_naive_workspace_size", "attn_naive_fwd", "attn_deviation_workspace_size",
            "attn_deviation", "attn_deviation_noalloc", "attn_decode_workspace_size", "attn_decode_fwd",
            "attn_bwd_workspace_size", "attn_bwd", "attn_emul_fwd", "attn_emul_round", "attn_status",
            "attn_strerror", "attn_last_variant", "attn_debug_wait_timeout")
@@ -61,6 +61,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_fwd_block_sparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp]
     lib.attn_fwd_block_sparse.restype = i
     lib.attn_fwd.restype = i
+    lib.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.attn_fwd_host_workspace_size.restype = sz
+    lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, vp, vp, sz, vp]
+    lib.attn_fwd_host.restype = i
     lib.attn_naive_workspace_size.argtypes = [i, i, i, i]
     lib.attn_naive_workspace_size.restype = sz
     lib.attn_naive_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, sz, vp]
@@ -164,37 +168,66 @@ def attn_fwd_block_sparse(q, k, v, block_mask, causal: bool = False, scale: floa
     return o, l
 
 
+def attn_fwd_host_workspace_size(B: int, H: int, N: int, d: int, dtype, with_mask: bool = False) -> int:
+    return int(lib.attn_fwd_host_workspace_size(B, H, N, d, _DTYPE[dtype] if not isinstance(dtype, int) else dtype,
+                                                int(bool(with_mask))))
+
+
+def _attn_fwd_host(q, k, v, causal, scale, Br, Bc, key_mask, out, lse, stream, want_lse, sync, workspace):
+    """attn_fwd on host tensors through the C ABI's attn_fwd_host: the library
+    copies the inputs into a device workspace, runs the forward and copies O
+    and LSE back, all on `stream`."""
+    for t in (q, k, v):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous host tensors")
+    if not (q.shape == k.shape == v.shape and q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPE:
+        raise ValueError("q, k, v must share shape and a supported dtype")
+    B, H, N, d = _shape4(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    if not isinstance(st, torch.cuda.Stream):
+        st = torch.cuda.ExternalStream(int(st))
+    m = None
+    if key_mask is not None:
+        m = key_mask
+        if m.device.type != "cpu" or m.dtype != torch.float32 or not m.is_contiguous() or m.numel() != B * H * N:
+            raise ValueError("key_mask must be a contiguous float32 host tensor with B*H*N elements")
+    need = attn_fwd_host_workspace_size(B, H, N, d, q.dtype, m is not None)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=torch.device("cuda", torch.cuda.current_device()))
+        workspace.record_stream(st)
+    ho = out if out is not None else torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    hl = lse if lse is not None else (torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+                                      if want_lse else None)
+    for t in (ho,) + ((hl,) if hl is not None else ()):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("out / lse must be contiguous host tensors")
+    rc = lib.attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(ho), _ptr(hl), B, H, N, d, int(bool(causal)), float(scale),
+                           int(Br), int(Bc), _DTYPE[q.dtype], _ptr(m), _ptr(workspace), workspace.numel(),
+                           ctypes.c_void_p(st.cuda_stream))
+    _check(rc, "attn_fwd_host")
+    if sync:
+        st.synchronize()
+    return ho, hl
+
+
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, Br: int = 0, Bc: int = 0,
-             key_mask=None, out=None, lse=None, stream=None, want_lse: bool = True, sync: bool = True):
+             key_mask=None, out=None, lse=None, stream=None, want_lse: bool = True, sync: bool = True,
+             workspace=None):
     """Tiled exact attention forward.  Returns (o, lse).
 
     Device tensors: the call is enqueued on `stream` (default: torch's current
-    stream) and returns immediately.  Host tensors (pinned or not): inputs are
-    copied to the current device, the kernel runs, and o / lse come back as
-    host tensors (end-to-end path), all on `stream`; with sync=False the call
-    returns once that work is enqueued (o / lse are valid after the stream is
-    synchronised), so calls on two streams overlap one's copies with the
-    other's kernel.
+    stream) and returns immediately.  Host tensors (pinned or not): the C ABI's
+    attn_fwd_host copies the inputs into a device workspace (``workspace``, a
+    uint8 device tensor of attn_fwd_host_workspace_size bytes, allocated here
+    if not given), runs the kernel and copies o / lse back into host tensors,
+    all on `stream`; with sync=False the call returns once that work is
+    enqueued (o / lse are valid after the stream is synchronised), so calls on
+    two streams overlap one's copies with the other's kernel.
     """
     if q.device.type == "cpu":
-        # End-to-end path from host memory.
-        dev = torch.device("cuda", torch.cuda.current_device())
-        st = stream if stream is not None else torch.cuda.current_stream()
-        if not isinstance(st, torch.cuda.Stream):
-            st = torch.cuda.ExternalStream(int(st))
-        with torch.cuda.stream(st):
-            qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
-            md = key_mask.to(dev, non_blocking=True) if key_mask is not None else None
-            o, l = attn_fwd(qd, kd, vd, causal, scale, Br, Bc, md, want_lse=want_lse, stream=st)
-            ho = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-            ho.copy_(o, non_blocking=True)
-            hl = None
-            if l is not None:
-                hl = lse if lse is not None else torch.empty(l.shape, dtype=l.dtype, pin_memory=True)
-                hl.copy_(l, non_blocking=True)
-        if sync:
-            st.synchronize()
-        return ho, hl
+        return _attn_fwd_host(q, k, v, causal, scale, Br, Bc, key_mask, out, lse, stream, want_lse, sync, workspace)
     for t in (q, k, v):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous tensors on one device")
@@ -224,16 +257,16 @@ def attn_naive_workspace_size(B: int, H: int, N: int, dtype) -> int:
 
 
 def attn_naive_fwd(q, k, v, causal: bool = False, scale: float | None = None, key_mask=None, workspace=None,
-                   stream=None):
+                   stream=None, out=None, lse=None):
     """Materialising baseline.  Returns (o, lse).  Allocates its workspace
-    with torch unless one is passed (uint8 device tensor)."""
+    (uint8 device tensor) and outputs with torch unless they are passed."""
     B, H, N, d = _shape4(q)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     need = attn_naive_workspace_size(B, H, N, q.dtype)
     ws = workspace if workspace is not None else torch.empty(need, dtype=torch.uint8, device=q.device)
-    o = torch.empty_like(q)
-    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    o = out if out is not None else torch.empty_like(q)
+    l = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     rc = lib.attn_naive_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, int(bool(causal)),
                             float(scale), _DTYPE[q.dtype], _ptr(key_mask), _ptr(ws), ws.numel(),
                             ctypes.c_void_p(_stream(stream)))

@@ -144,6 +144,79 @@ int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, i
     return rc;
 }
 
+namespace {
+// attn_fwd_host's device workspace: Q | K | V | O | LSE | key mask, each at a
+// 256-byte boundary.
+struct HostLayout {
+    size_t q, k, v, o, lse, mask, total;
+};
+HostLayout host_layout(int B, int H, int N, int d, size_t es, bool with_mask) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t t = static_cast<size_t>(B) * H * N * d * es;
+    const size_t r = static_cast<size_t>(B) * H * N * 4;
+    HostLayout L;
+    size_t off = 0;
+    L.q = off; off += up(t);
+    L.k = off; off += up(t);
+    L.v = off; off += up(t);
+    L.o = off; off += up(t);
+    L.lse = off; off += up(r);
+    L.mask = off; off += with_mask ? up(r) : 0;
+    L.total = off;
+    return L;
+}
+}  // namespace
+
+size_t attn_fwd_host_workspace_size(int B, int H, int N, int d, int dtype, int with_mask) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+    if (static_cast<long long>(B) * H * N >= (1LL << 31) || static_cast<long long>(N) * d >= (1LL << 31)) return 0;
+    const size_t es = dtype == ATTN_F32 ? 4 : dtype == ATTN_BF16 ? 2 : 0;
+    if (!es) return 0;
+    return host_layout(B, H, N, d, es, with_mask != 0).total;
+}
+
+int attn_fwd_host(const void *Qh, const void *Kh, const void *Vh, void *Oh, float *LSEh, int B, int H, int N, int d,
+                  int causal, float scale, int Br, int Bc, int dtype, const float *key_mask_h, void *workspace,
+                  size_t ws_bytes, void *stream) {
+    if (!Qh || !Kh || !Vh || !Oh) return kErrArg;
+    const size_t need = attn_fwd_host_workspace_size(B, H, N, d, dtype, key_mask_h != nullptr);
+    if (need == 0) return (dtype == ATTN_F32 || dtype == ATTN_BF16) ? kErrArg : kErrUnsupported;
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return kErrWorkspace;
+    char *ws = static_cast<char *>(workspace);
+    const HostLayout L = host_layout(B, H, N, d, dtype == ATTN_F32 ? 4 : 2, key_mask_h != nullptr);
+    const size_t t = static_cast<size_t>(B) * H * N * d * (dtype == ATTN_F32 ? 4 : 2);
+    const size_t r = static_cast<size_t>(B) * H * N * 4;
+    // Dry run of the argument checks on the device buffers (a zero-size O
+    // would be rejected by the same checks): nothing is enqueued on an
+    // invalid argument.
+    int rc = check_common(ws + L.q, ws + L.k, ws + L.v, ws + L.o, B, H, N, d, scale,
+                          key_mask_h ? reinterpret_cast<const float *>(ws + L.mask) : nullptr);
+    if (rc != kOk) return rc;
+    if (causal != 0 && causal != 1) return kErrArg;
+    if (dtype == ATTN_BF16) {
+        if (d != 64 && d != 128) return kErrUnsupported;
+        if (!((Br == 0 || Br == 64 || Br == 128) && (Bc == 0 || Bc == 64 || Bc == 128 || Bc == 256)))
+            return kErrUnsupported;
+    } else {
+        if (d > 128) return kErrUnsupported;
+        if (!((Br == 0 || Br == 64) && (Bc == 0 || Bc == 64))) return kErrUnsupported;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(ws + L.q, Qh, t, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(ws + L.k, Kh, t, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(ws + L.v, Vh, t, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        (key_mask_h && cudaMemcpyAsync(ws + L.mask, key_mask_h, r, cudaMemcpyHostToDevice, st) != cudaSuccess))
+        return kErrCuda;
+    rc = attn_fwd(ws + L.q, ws + L.k, ws + L.v, ws + L.o, LSEh ? reinterpret_cast<float *>(ws + L.lse) : nullptr, B,
+                  H, N, d, causal, scale, Br, Bc, dtype,
+                  key_mask_h ? reinterpret_cast<const float *>(ws + L.mask) : nullptr, stream);
+    if (rc != kOk) return rc;
+    if (cudaMemcpyAsync(Oh, ws + L.o, t, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        (LSEh && cudaMemcpyAsync(LSEh, ws + L.lse, r, cudaMemcpyDeviceToHost, st) != cudaSuccess))
+        return kErrCuda;
+    return kOk;
+}
+
 int attn_fwd_block_sparse(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
                           int d, int causal, float scale, int dtype, const unsigned char *block_mask,
                           const float *key_mask, void *stream) {

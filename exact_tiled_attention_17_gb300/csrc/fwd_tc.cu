@@ -39,8 +39,10 @@
 // moves m to the row's maximum and is redone.  Exact up to rounding because
 // O / l does not depend on the reference point, and every p stays <= 2^16.
 // The two warpgroups of a tile take this decision together.
-// One denominator per row, the float32 sum of p: it normalises O (whose P V
-// uses p rounded to bf16) and gives the LSE.
+// One denominator per row, the float32 sum of the bf16-rounded p that P V
+// applies, so the weights that reach O sum to one (a row whose weight sits
+// on one key gets that key's V exactly, wherever the reference maximum is);
+// it also gives the LSE.
 //
 // Block-sparse variant (BSPARSE): a byte mask over 128 x 128 (query block, key
 // block) pairs says which blocks take part; every other score is -inf.  The
@@ -560,7 +562,11 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         constexpr int CW = BC / S::NH;       // S columns of this warpgroup
         constexpr int OC = D / 32 / S::NH;   // 32-column chunks of O of this warpgroup
         float m = kNegInf;    // reference maximum, log2 units (the same in both warpgroups)
-        float l = 0.f;        // sum of float32 p over this warpgroup's columns
+        float l = 0.f;        // sum of the bf16-rounded p over this warpgroup's columns
+        // The previous tile needed its maximum and moved the reference: take
+        // this tile's maximum first instead of guessing (the same for every
+        // warp that shares the tile's rows).
+        bool max_first = false;
         bool ok = true;
         // per-row exchange slot of warpgroup hh of this tile; barrier of the pair
         auto xch = [&](int hh) -> uint32_t { return sbase + S::OFF_XCH + ((q * 2 + hh) * 128 + row_in) * 8; };
@@ -595,9 +601,11 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             // past N; double-buffered so one barrier per tile suffices.
             const float *msm = reinterpret_cast<const float *>(smem + S::OFF_MASK) + (q * 2 + (j & 1)) * BC;
             if constexpr (MASKED) {
+                // Staged by all 128 threads of the warpgroup (with M = 64 two
+                // lanes share a row, so the row index would cover only half).
                 float *mw = reinterpret_cast<float *>(smem + S::OFF_MASK) + (q * 2 + (j & 1)) * BC;
 #pragma unroll
-                for (int t = h * CW + row_in; t < (h + 1) * CW; t += 128) {
+                for (int t = h * CW + wq * 32 + lane; t < (h + 1) * CW; t += 128) {
                     const int key = key0 + t;
                     mw[t] = (key < N) ? __ldg(mrow + key) * kLog2e : kNegInf;
                 }
@@ -642,9 +650,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             // p = 2^(x - m_use) for one chunk, packed to bf16 pairs and written
             // over S's first BC/2 columns (chunk c -> columns 16c .. 16c+15,
             // never ahead of the chunks still to be read).
-            // Partial sums per chunk keep the add chains short: ls2 sums the
-            // float32 p as float32 pairs.
-            auto exp_chunk = [&](int c, const uint32_t *r, uint64_t negm2, uint64_t &ls2) {
+            // Partial sums per chunk keep the add chains short: sa / sb sum the
+            // bf16-rounded p of the even / odd columns.
+            auto exp_chunk = [&](int c, const uint32_t *r, uint64_t negm2, float &sa, float &sb) {
                 const uint64_t sl2x2 = f2_pack(sl2, sl2);
                 uint32_t pk[16];
 #pragma unroll
@@ -657,7 +665,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                     uint32_t w = pack_bf16x2(p0, p1);
                     if (!active) w = 0u;
                     pk[e] = w;
-                    ls2 = f2_add(ls2, f2_pack(p0, p1));
+                    add_bf16x2_f32(sa, sb, w);
                 }
                 tmem_st16(tS + 16 * c, pk);
             };
@@ -740,7 +748,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                         if (g + 1 < NG) issue_group(g + 1, sbuf[(g + 1) & 1]);
 #pragma unroll
                         for (int c = 0; c < HC / 32; ++c) {
-                            uint64_t ls2 = f2_pack(0.f, 0.f);
+                            float sa = 0.f, sb = 0.f;
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const float x0 = __uint_as_float(sr[32 * c + 2 * e]);
@@ -755,11 +763,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                                 uint32_t w = pack_bf16x2(p0, p1);
                                 if (!active) w = 0u;
                                 pk[(HC / 2) * g + 16 * c + e] = w;
-                                ls2 = f2_add(ls2, f2_pack(p0, p1));
+                                add_bf16x2_f32(sa, sb, w);
                             }
-                            float s0, s1;
-                            f2_unpack(ls2, s0, s1);
-                            ls += s0 + s1;
+                            ls += sa + sb;
                         }
                         if (g + 1 < NG) {
                             tmem_ld_wait();
@@ -790,36 +796,42 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                     }
                     return mx;
                 };
-                // Exponentiate against the current reference with no maximum.
-                // A row whose sum exceeds kFastSumLimit (or overflows, or has
-                // no finite reference yet) has a score far past the reference:
-                // only then is the tile's maximum taken, the reference moved
-                // and the tile redone (S is still intact: P is written after).
-                // The first tile of a row has no reference: maximum first.
+                // Guess: exponentiate against the current reference with no
+                // maximum.  A row whose sum exceeds kFastSumLimit (or
+                // overflows, or has no finite reference yet) has a score far
+                // past the reference: only then is the tile's maximum taken,
+                // the reference moved and the tile redone (S is still intact:
+                // P is written after).  The first tile of a row, and a tile
+                // after one that moved the reference, take the maximum first.
+                // Either way the reference moves only to a maximum more than
+                // kRescaleThresh above it, so every p stays below 2^16.
+                const bool guess = j > 0 && !max_first;
                 float ls = 0.f;
-                bool need = active;
-                if (j > 0) {
+                bool redo = true;
+                if (guess) {
                     exps(m, ls);
-                    need = active && !(ls <= kFastSumLimit);
+                    const bool need = active && !(ls <= kFastSumLimit);
+                    if constexpr (S::NH == 2) redo = named_bar_red_or(7 + q, 256, need);
+                    else redo = __any_sync(0xffffffffu, need);
                 }
-                bool redo;
-                if constexpr (S::NH == 2) redo = named_bar_red_or(7 + q, 256, need);
-                else redo = __any_sync(0xffffffffu, need);
                 if (redo) {
                     float mx = cols_max();
-                    bool need_row = need;
                     if constexpr (S::NH == 2) {
-                        float mo, no;
-                        exchange(mx, need ? 1.f : 0.f, mo, no);
+                        float mo, unused;
+                        exchange(mx, 0.f, mo, unused);
                         mx = fmaxf(mx, mo);
-                        need_row = need || (no != 0.f);
                     }
-                    const float m_new = need_row ? fmaxf(m, mx) : m;
-                    const float a = (m_new == m) ? 1.f : ex2(m - m_new);   // m = -inf: nothing to scale
-                    if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+                    // (m = -inf: any finite maximum is taken; nothing to scale)
+                    const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
+                    const bool moved = m_new != m;
+                    const float a = moved ? ex2(m - m_new) : 1.f;
+                    if (j > 0 && __any_sync(0xffffffffu, moved)) {
                         o_settled();
                         rescale_o(a);
                     }
+                    // (the first tile's move from -inf says nothing about the next)
+                    if constexpr (S::NH == 2) max_first = named_bar_red_or(7 + q, 256, j > 0 && moved);
+                    else max_first = __any_sync(0xffffffffu, j > 0 && moved);
                     m = m_new;
                     l *= a;
                     exps(m == kNegInf ? 0.f : m, ls);
@@ -862,11 +874,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                     tmem_ld_wait();
                     reg_fence32(sr);
                     if (edge) mask_chunk(c, sr);
-                    uint64_t ls2 = f2_pack(0.f, 0.f);
-                    exp_chunk(c, sr, negm2, ls2);
-                    float s0, s1;
-                    f2_unpack(ls2, s0, s1);
-                    tile_ls += s0 + s1;
+                    float sa = 0.f, sb = 0.f;
+                    exp_chunk(c, sr, negm2, sa, sb);
+                    tile_ls += sa + sb;
                 }
                 l = l * alpha + tile_ls;
                 release_p();

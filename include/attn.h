@@ -82,6 +82,30 @@ int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
              int dtype, const float *key_mask, void *stream);
 
 /*
+ * attn_fwd_host — attn_fwd on host memory: the same computation ("Is Flash
+ * Attention Stable?" §II-A), for a caller whose Q, K, V live in host memory
+ * (the end-to-end path: inputs in, results out).  On `stream` it copies Q, K,
+ * V (and the key mask) into `workspace`, runs attn_fwd there, and copies O
+ * (and LSE) back.
+ *
+ * Qh, Kh, Vh: host [B][H][N][d] of `dtype`; Oh: host [B][H][N][d] of `dtype`
+ * (written); LSEh: host [B][H][N] float32 (written) or NULL; key_mask_h: host
+ * [B][H][N] float32 additive mask or NULL.  All host buffers are the
+ * caller's; page-locked (pinned) memory lets the copies overlap other work,
+ * pageable memory also works but the copies then wait for the host.
+ * workspace: device memory of at least attn_fwd_host_workspace_size(B, H, N,
+ * d, dtype, key_mask_h != NULL) bytes, 256-byte aligned, owned by the caller
+ * and holding the device copies while the call runs.  Other arguments and
+ * errors as for attn_fwd; argument errors are returned before anything is
+ * enqueued.  Asynchronous: Oh / LSEh hold the result once `stream` has been
+ * synchronised, and the host buffers must stay valid until then.
+ */
+size_t attn_fwd_host_workspace_size(int B, int H, int N, int d, int dtype, int with_mask);
+int attn_fwd_host(const void *Qh, const void *Kh, const void *Vh, void *Oh, float *LSEh, int B, int H, int N, int d,
+                  int causal, float scale, int Br, int Bc, int dtype, const float *key_mask_h, void *workspace,
+                  size_t ws_bytes, void *stream);
+
+/*
  * attn_fwd_block_sparse — the forward of attn_fwd restricted to marked blocks
  * of the score matrix.  The yadro-code.ru FlashAttention tutorial notes that
  * the method's paper also treats a block-sparse extension; read plainly, a

@@ -2,10 +2,14 @@
 
 run_case() runs attn_fwd through the C ABI on seeded (or given) inputs and
 compares O and LSE with the FP64 oracle, element by element: max-abs on O of
-1e-5 for float32 inputs and 2e-2 for bf16 inputs with float32 accumulation;
-LSE within float32 rounding of the scaled scores, |dLSE| <= 1e-5 * max(1,
-|LSE|) for float32 and 1e-3 + 2e-6 * |LSE| for bf16.  Fully masked rows
-must give O == 0 exactly and LSE == -inf, and no output may be NaN.
+1e-5 for float32 inputs and 2e-2 for bf16 inputs with float32 accumulation.
+LSE: |dLSE| <= 1e-5 * max(1, |LSE|) for float32 (float32 rounding of the
+scaled scores).  For bf16, |dLSE| <= 1e-3 + 2^-8 + 2e-6 * |LSE|.  The
+2e-6 * |LSE| term covers float32 scores up to ~1e4.  The 2^-8 term covers
+the denominator: it sums the p rounded to bf16 (the weights O applies), each
+within a relative 2^-8 of p, so its log is within ln(1 + 2^-8) < 2^-8 of the
+exact one.  Fully masked rows must give O == 0 exactly and LSE == -inf, and
+no output may be NaN.
 """
 import math
 
@@ -20,7 +24,7 @@ TOL_O = {"f32": 1e-5, "bf16": 2e-2}
 
 def _lse_tol(dtype, ref):
     a = np.abs(np.where(np.isfinite(ref), ref, 0.0))
-    return 1e-5 * np.maximum(1.0, a) if dtype == "f32" else 1e-3 + 2e-6 * a
+    return 1e-5 * np.maximum(1.0, a) if dtype == "f32" else 1e-3 + 2.0 ** -8 + 2e-6 * a
 
 
 def run_case(eta, B, H, N, d, dtype, causal, Br=0, Bc=0, mask=None, qk_scale=1.0, seed=0, rows=None,

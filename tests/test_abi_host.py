@@ -174,3 +174,42 @@ def test_backward_and_block_sparse_rejection(lib):
     assert bs(dtype=0) == -2
     assert bs(d=96) == -2
     assert bs(N=131073) == -2
+
+
+def test_host_entry_sizes_and_rejection(lib):
+    """attn_fwd_host: workspace arithmetic, and argument errors returned
+    before any copy is enqueued (fake, never dereferenced pointers)."""
+    vp = ctypes.c_void_p
+    ws_size = lib.attn_fwd_host_workspace_size
+    ws_size.restype = ctypes.c_size_t
+    ws_size.argtypes = [ctypes.c_int] * 6
+    t = 2 * 16 * 4096 * 128 * 2                       # one bf16 tensor of the bench shape
+    r = 2 * 16 * 4096 * 4                             # one float32 row vector
+    assert ws_size(2, 16, 4096, 128, 1, 0) == 4 * t + r
+    assert ws_size(2, 16, 4096, 128, 1, 1) == 4 * t + 2 * r
+    assert ws_size(1, 1, 3, 5, 0, 0) == 4 * 256 + 256  # every part on a 256-byte boundary
+    assert ws_size(1, 1, 8, 64, 2, 0) == 0             # float64 is not a forward dtype
+    assert ws_size(0, 1, 8, 64, 1, 0) == 0
+    f = lib.attn_fwd_host
+    f.restype = ctypes.c_int
+    f.argtypes = [vp] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float] + [ctypes.c_int] * 3 + [vp, vp, ctypes.c_size_t, vp]
+    p, big = vp(256), 1 << 30
+
+    def host(**kw):
+        a = dict(Q=p, O=p, N=8, d=64, causal=0, scale=0.125, Br=0, Bc=0, dtype=1, ws=p, ws_bytes=big)
+        a.update(kw)
+        return f(a["Q"], p, p, a["O"], None, 1, 1, a["N"], a["d"], a["causal"], a["scale"], a["Br"], a["Bc"],
+                 a["dtype"], None, a["ws"], a["ws_bytes"], None)
+
+    assert host(Q=None) == -1
+    assert host(O=None) == -1
+    assert host(N=0) == -1
+    assert host(scale=0.0) == -1
+    assert host(causal=2) == -1
+    assert host(ws=None) == -3
+    assert host(ws_bytes=1000) == -3
+    assert host(ws=vp(256 + 16)) == -3               # not 256-byte aligned
+    assert host(d=96) == -2                          # bf16: d in {64, 128}
+    assert host(Bc=96) == -2
+    assert host(dtype=2) == -2
+    assert host(dtype=0, Br=128) == -2

@@ -3,7 +3,8 @@ oracle's block-sparse reading: scores outside the marked 128 x 128
 (query block, key block) pairs are -inf before the softmax.
 
 Tolerances are those of the bf16 forward: O max-abs 2e-2, LSE
-1e-3 + 2e-6 |LSE|; rows that see no allowed key give O = 0, LSE = -inf."""
+1e-3 + 2^-8 + 2e-6 |LSE| (the forward's bf16 LSE bound); rows that see no allowed key give O = 0,
+LSE = -inf."""
 import math
 
 import numpy as np
@@ -42,7 +43,7 @@ def _check(eta, B, H, N, d, causal, bm, seed, key_mask=None, rows=None):
     assert np.array_equal(np.isneginf(lg), inf_ref)
     assert np.all(og[inf_ref] == 0.0)
     fin = ~inf_ref
-    assert np.all(np.abs(lg[fin] - l_ref[fin]) <= 1e-3 + 2e-6 * np.abs(l_ref[fin]))
+    assert np.all(np.abs(lg[fin] - l_ref[fin]) <= 1e-3 + 2.0 ** -8 + 2e-6 * np.abs(l_ref[fin]))
     return inf_ref
 
 

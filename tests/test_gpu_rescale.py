@@ -19,7 +19,7 @@ ln 2 so that a score is its own log2-domain value).  They also run the
 adversarial workload's generator (Q and K x30, -inf key padding, fully
 masked rows) through every variant and through the K/V-split cluster tail.
 Bar: the forward's bf16 tolerance against the FP64 oracle (O max-abs 2e-2;
-LSE 1e-3 + 2e-6 |LSE|; fully masked rows O = 0, LSE = -inf).
+LSE 1e-3 + 2^-8 + 2e-6 |LSE|; fully masked rows O = 0, LSE = -inf).
 """
 import math
 
