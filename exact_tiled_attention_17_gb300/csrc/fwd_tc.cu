@@ -33,12 +33,12 @@
 // BR = 64 uses M = 64 MMAs, whose accumulator rows r sit in tensor-memory lane
 // 32*(r/16) + r%16: lanes 0..15 of each warp carry rows, lanes 16..31 idle.
 //
-// The reference maximum m is set from a row's first tile.  Later tiles are
-// exponentiated against m without computing their maximum; only a tile whose
-// p sum passes kFastSumLimit = 2^16 (or that has no finite reference yet)
-// moves m to the row's maximum and is redone.  Exact up to rounding because
-// O / l does not depend on the reference point, and every p stays <= 2^16.
-// The two warpgroups of a tile take this decision together.
+// Each tile's row maximum is taken first (with the tensor-memory loads of S,
+// which return it on sm_103a; the two warpgroups of a tile exchange theirs),
+// then the exponentials.  The reference maximum m moves only to a tile
+// maximum more than kRescaleThresh above it, so O is rescaled rarely and
+// every p stays below 2^kRescaleThresh.
+// Exact up to rounding: O / l does not depend on the reference point.
 // One denominator per row, the float32 sum of the bf16-rounded p that P V
 // applies, so the weights that reach O sum to one (a row whose weight sits
 // on one key gets that key's V exactly, wherever the reference maximum is);
@@ -50,8 +50,12 @@
 // list built at the start); a listed tile that is not marked for a query tile
 // is masked whole for it.
 #include <cuda_bf16.h>
-#include <type_traits>
+
+#include <algorithm>
+#include <atomic>
 #include <cstdio>
+#include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -62,9 +66,6 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThresh = 8.0f;
-// A tile whose p = 2^(x - m) sum to at most this needs no move of the
-// reference maximum: every p is at most the sum.
-constexpr float kFastSumLimit = 65536.0f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
 constexpr int kBsListCap = 1024;   // key tiles a block-sparse CTA can list (N <= 131072)
@@ -100,9 +101,6 @@ struct TcShape {
     static constexpr int SOFTMAX_WARPS = 4 * NQ * NH;
     static constexpr int WARP_TMA = SOFTMAX_WARPS;
     static constexpr int WARP_MMA = SOFTMAX_WARPS + 1;
-    // Two query tiles: a full extra warpgroup (TMA, MMA, 2 idle) so that
-    // setmaxnreg can move registers between whole warpgroups.
-    static constexpr bool SPLIT_REGS = (NQ == 2);
 
     // setmaxnreg could move registers from the producer/MMA warpgroup to the
     // softmax warpgroups; every shape here fits the launch share, and the
@@ -122,7 +120,7 @@ struct TcShape {
     static constexpr int OFF_LIST = OFF_XCH + XCH_BYTES;
     static constexpr int OFF_BAR = OFF_LIST + LIST_BYTES;
     // barriers: q_full[NQ] full[NS] empty[NS] s_full[NQ][NSB] p_full[NQ][NSB][NH] o_full[NQ]
-    // pv_done[NQ] done part done_read
+    // pv_done[NQ] q_free[NQ] o_free[NQ] done part
     static constexpr int BAR_QFULL = 0;
     static constexpr int BAR_FULL = BAR_QFULL + NQ;
     static constexpr int BAR_EMPTY = BAR_FULL + NS;
@@ -130,7 +128,11 @@ struct TcShape {
     static constexpr int BAR_PFULL = BAR_SFULL + NQ * NSB;
     static constexpr int BAR_OFULL = BAR_PFULL + NQ * NSB * NH;
     static constexpr int BAR_PVDONE = BAR_OFULL + NQ;   // two S buffers: each P_q V has completed
-    static constexpr int BAR_DONE = BAR_PVDONE + NQ;
+    // A CTA runs several work units: Q_q may be reloaded once the unit's last
+    // S_q product has completed, and O_q rewritten once the epilogue has read it.
+    static constexpr int BAR_QFREE = BAR_PVDONE + NQ;
+    static constexpr int BAR_OFREE = BAR_QFREE + NQ;
+    static constexpr int BAR_DONE = BAR_OFREE + NQ;
     static constexpr int BAR_PART = BAR_DONE + 1;       // split K/V: partials of the other parts are ready
     static constexpr int NBARS = BAR_PART + 1;
     // split K/V: a part's partial results, staged in the (then idle) Q tiles and K/V ring:
@@ -170,60 +172,93 @@ struct TcParams {
     const float *key_mask;  // [BH][N] additive, or null
     const uint8_t *block_mask;  // block-sparse: [BH][nkb][nkb] bytes, non-zero = take part
     int nkb;                    // 128-row blocks per head
+    __nv_bfloat16 *o;       // [BH][N][D]
     float *lse;             // [BH][N], or null
     int *err;               // device error word
-    // Work items (groups of NQ query tiles) are numbered in launch order.
-    // Items [0, n_full) run whole; every later item is split along K/V into
-    // `split` parts run by the `split` CTAs of one cluster, merged by part 0.
+    // Work items (groups of NQ query tiles of one head) are numbered heaviest
+    // first for causal (largest rows first) and head-major otherwise.  Every
+    // CTA of the grid (G CTAs, at most one per SM) runs a list of work units:
+    // items [0, n_full) whole, CTA c taking items c, c + G, c + 2G, ...
+    // (causal: every other round in reverse, so long and short items mix);
+    // then each item in [n_full, items) split along K/V into `split` parts,
+    // run as the last unit of the `split` CTAs of one cluster and merged by
+    // part 0.
+    int items;
     int n_full;
     int split;
+    int split_shift;   // log2(split)
 };
+
+// The u-th work unit of CTA c in a grid of G CTAs (see TcParams); false when
+// the CTA has no u-th unit.
+__device__ __forceinline__ bool work_unit(const TcParams &p, int c, int G, int u, int &item, int &part,
+                                          int &nparts) {
+    auto full = [&](int r) { return r * G + ((p.causal && (r & 1)) ? G - 1 - c : c); };
+    const int f = full(u);
+    if (f < p.n_full) {
+        item = f;
+        part = 0;
+        nparts = 1;
+        return true;
+    }
+    if (u > 0 && full(u - 1) >= p.n_full) return false;   // the tail unit comes right after the full ones
+    if (c >= (p.items - p.n_full) << p.split_shift) return false;
+    item = p.n_full + (c >> p.split_shift);
+    part = c & (p.split - 1);   // equals the rank in the cluster
+    nparts = p.split;
+    return true;
+}
 
 template <int D, int BR, int BC, int NQ, bool MASKED, bool BSPARSE>
 __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                       const TcParams p) {
+                       const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
     using S = TcShape<D, BR, BC, NQ, MASKED, BSPARSE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- work item ----
-    // Causal: heaviest query groups (largest rows) first.  Non-causal: all
-    // query groups of one head together, so a head's K/V stay hot in L2.
-    const int lin = blockIdx.x;
-    int item = lin, part = 0, nparts = 1;
-    if (lin >= p.n_full) {
-        const int t = lin - p.n_full;
-        item = p.n_full + t / p.split;
-        part = t % p.split;   // equals the rank in the cluster
-        nparts = p.split;
-    }
-    const int qg = p.causal ? p.num_qg - 1 - item / p.BH : item % p.num_qg;
-    const int bh = p.causal ? item % p.BH : item / p.num_qg;
     const int N = p.N;
     const int nkv_all = (N + BC - 1) / BC;
-    // this CTA's K/V tiles: [kv_lo, kv_lo + nkv) (a part's share of a split item)
-    const int kv_lo = static_cast<int>((static_cast<long long>(nkv_all) * part) / nparts);
-    const int kv_hi = static_cast<int>((static_cast<long long>(nkv_all) * (part + 1)) / nparts);
+    const int cta = blockIdx.x;
+    const int G = gridDim.x;
+    uint16_t *kv_list = reinterpret_cast<uint16_t *>(smem + S::OFF_LIST);
+
+    // ---- geometry of one work unit ----
+    // Causal: heaviest query groups (largest rows) first.  Non-causal: all
+    // query groups of one head together, so a head's K/V stay hot in L2.
+    // Query tile q starts at row r0[q] and runs the K/V tiles
+    // [kv_lo, kv_lo + nkv[q]) (a part's share of a split item; block-sparse:
+    // the first nkv[q] entries of the CTA's list).
+    int bh = 0, kv_lo = 0, nkv_max = 0;
     int r0[NQ], nkv[NQ];
-    int nkv_max = 0;
+    // (32-bit arithmetic only: nkv_all * 8 < 2^31, and nparts = 2^split_shift)
+    auto geometry = [&](int item, int part, int nparts) {
+        const int dq = p.causal ? p.BH : p.num_qg;
+        const int quo = item / dq, rem = item - quo * dq;
+        const int qg = p.causal ? p.num_qg - 1 - quo : rem;
+        bh = p.causal ? rem : quo;
+        const int sh = nparts > 1 ? p.split_shift : 0;
+        kv_lo = (nkv_all * part) >> sh;
+        const int kv_hi = (nkv_all * (part + 1)) >> sh;
+        nkv_max = 0;
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        r0[q] = (qg * NQ + q) * BR;
-        if (r0[q] >= N) {
-            nkv[q] = 0;
-        } else if (p.causal) {
-            const int last_row = min(r0[q] + BR - 1, N - 1);
-            nkv[q] = min(nkv_all, last_row / BC + 1);
-        } else {
-            nkv[q] = kv_hi - kv_lo;
+        for (int q = 0; q < NQ; ++q) {
+            r0[q] = (qg * NQ + q) * BR;
+            if (r0[q] >= N) {
+                nkv[q] = 0;
+            } else if constexpr (BSPARSE) {
+                nkv[q] = reinterpret_cast<const int *>(smem + S::OFF_LIST + kBsListCap * 2)[q];
+            } else if (p.causal) {
+                const int last_row = min(r0[q] + BR - 1, N - 1);
+                nkv[q] = min(nkv_all, last_row / BC + 1);
+            } else {
+                nkv[q] = kv_hi - kv_lo;
+            }
+            nkv_max = max(nkv_max, nkv[q]);
         }
-        nkv_max = max(nkv_max, nkv[q]);
-    }
+    };
 
     auto bar = [&](int i) -> uint32_t { return sbase + S::OFF_BAR + 8 * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::OFF_MISC);
@@ -240,13 +275,15 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             }
             mbar_init(bar(S::BAR_OFULL + q), 1);
             mbar_init(bar(S::BAR_PVDONE + q), 1);
+            mbar_init(bar(S::BAR_QFREE + q), 1);
+            mbar_init(bar(S::BAR_OFREE + q), 128 * S::NH);
         }
         for (int s = 0; s < S::NS; ++s) {
             mbar_init(bar(S::BAR_FULL + s), 1);
             mbar_init(bar(S::BAR_EMPTY + s), 1);
         }
         mbar_init(bar(S::BAR_DONE), 1);
-        mbar_init(bar(S::BAR_PART), static_cast<uint32_t>((nparts > 1 ? nparts - 1 : 1) * S::SOFTMAX_WARPS * 32));
+        mbar_init(bar(S::BAR_PART), static_cast<uint32_t>((p.split > 1 ? p.split - 1 : 1) * S::SOFTMAX_WARPS * 32));
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -254,8 +291,14 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
         tmem_relinquish();
     }
-    uint16_t *kv_list = reinterpret_cast<uint16_t *>(smem + S::OFF_LIST);
     if constexpr (BSPARSE) {
+        // One work unit per CTA (the launch makes one CTA per item).
+        int item0 = 0, part0 = 0, nparts0 = 1;
+        work_unit(p, cta, G, 0, item0, part0, nparts0);
+        const int qg = p.causal ? p.num_qg - 1 - item0 / p.BH : item0 % p.num_qg;
+        bh = p.causal ? item0 % p.BH : item0 / p.num_qg;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) r0[q] = (qg * NQ + q) * BR;
         // Warp 1 lists the key tiles marked for at least one of the CTA's query
         // tiles (in order, with the per-tile marks in bits 14..15) and, per
         // query tile, how many list entries reach its last marked tile.  A
@@ -305,16 +348,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    if constexpr (BSPARSE) {
-        const int *counts = reinterpret_cast<const int *>(smem + S::OFF_LIST + kBsListCap * 2);
-        nkv_max = 0;
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            nkv[q] = counts[q];
-            nkv_max = max(nkv_max, nkv[q]);
-        }
-    }
-    // first key of the CTA's j-th K/V tile
+    // first key tile of the unit's j-th K/V tile
     auto kv_tile = [&](int jj) -> int {
         if constexpr (BSPARSE) return kv_list[jj] & 0x3FFF;
         else return kv_lo + jj;
@@ -322,7 +356,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
     if constexpr (S::CAN_SPLIT) {
         // Parts of a split item arrive on each other's barriers: all of the
         // cluster's barriers must be initialised first.
-        if (nparts > 1) cluster_sync();
+        if (p.split > 1) cluster_sync();
     }
 
     if (warp >= S::SOFTMAX_WARPS) {
@@ -344,42 +378,55 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                 tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(&tm_k);
                 tma_prefetch_desc(&tm_v);
-                tma_prefetch_desc(&tm_o);
             }
             const uint64_t pol_kv = l2_policy_evict_last();   // K/V are re-read by every query group
             const uint64_t pol_q = l2_policy_evict_first();   // Q is read once
-            for (int q = 0; q < NQ; ++q) {
-                if (nkv[q] == 0) continue;
-                if (leader) {
-                    mbar_arrive_expect_tx(bar(S::BAR_QFULL + q), S::Q_BYTES);
+            int t = 0;                 // K/V tiles issued so far, all units: K_0 V_0 K_1 V_1 ...
+            int uo[NQ];                // units so far in which query tile q ran
 #pragma unroll
-                    for (int cb = 0; cb < S::CB; ++cb)
-                        tma_load_3d_hint(sQ + q * S::Q_BYTES + cb * (BR * 128), &tm_q, bar(S::BAR_QFULL + q),
-                                         cb * 64, r0[q], bh, pol_q);
-                }
-            }
-            const int T = 2 * nkv_max;  // K_0 V_0 K_1 V_1 ...
-            int issued = 0;
-            for (int t = 0; t < T; ++t) {
-                const int slot = t % S::NS, round = t / S::NS;
-                if (round > 0 && !wwait(bar(S::BAR_EMPTY + slot), (round - 1) & 1, 1)) break;
-                if (leader) {
-                    mbar_arrive_expect_tx(bar(S::BAR_FULL + slot), S::SLOT_BYTES);
-                    const CUtensorMap *m = (t & 1) ? &tm_v : &tm_k;
-                    const int j = t >> 1;
+            for (int q = 0; q < NQ; ++q) uo[q] = 0;
+            bool ok = true;
+            for (int u = 0; ok; ++u) {
+                int item, part, nparts;
+                if (!work_unit(p, cta, G, u, item, part, nparts)) break;
+                geometry(item, part, nparts);
 #pragma unroll
-                    for (int cb = 0; cb < S::CB; ++cb)
-                        tma_load_3d_hint(sRing + slot * S::SLOT_BYTES + cb * (BC * 128), m,
-                                         bar(S::BAR_FULL + slot), cb * 64, kv_tile(j) * BC, bh, pol_kv);
+                for (int q = 0; q < NQ; ++q) {
+                    if (nkv[q] == 0) continue;
+                    // Q_q of the previous unit is still read by its last S products.
+                    if (uo[q] > 0 && !wwait(bar(S::BAR_QFREE + q), (uo[q] - 1) & 1, 4)) ok = false;
+                    if (ok && leader) {
+                        mbar_arrive_expect_tx(bar(S::BAR_QFULL + q), S::Q_BYTES);
+#pragma unroll
+                        for (int cb = 0; cb < S::CB; ++cb)
+                            tma_load_3d_hint(sQ + q * S::Q_BYTES + cb * (BR * 128), &tm_q, bar(S::BAR_QFULL + q),
+                                             cb * 64, r0[q], bh, pol_q);
+                    }
+                    ++uo[q];
                 }
-                issued = t + 1;
+                for (int tt = 0; ok && tt < 2 * nkv_max; ++tt, ++t) {
+                    const int slot = t % S::NS, round = t / S::NS;
+                    if (round > 0 && !wwait(bar(S::BAR_EMPTY + slot), (round - 1) & 1, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) {
+                        mbar_arrive_expect_tx(bar(S::BAR_FULL + slot), S::SLOT_BYTES);
+                        const CUtensorMap *m = (tt & 1) ? &tm_v : &tm_k;
+#pragma unroll
+                        for (int cb = 0; cb < S::CB; ++cb)
+                            tma_load_3d_hint(sRing + slot * S::SLOT_BYTES + cb * (BC * 128), m,
+                                             bar(S::BAR_FULL + slot), cb * 64, kv_tile(tt >> 1) * BC, bh, pol_kv);
+                    }
+                }
             }
             // Drain: every copy this warp started has landed before the CTA
             // may exit (normally already true).
-            for (int t = max(0, issued - S::NS); t < issued; ++t)
-                wwait(bar(S::BAR_FULL + t % S::NS), (t / S::NS) & 1, 2);
+            for (int tt = max(0, t - S::NS); tt < t; ++tt)
+                wwait(bar(S::BAR_FULL + tt % S::NS), (tt / S::NS) & 1, 2);
+#pragma unroll
             for (int q = 0; q < NQ; ++q)
-                if (nkv[q] > 0) wwait(bar(S::BAR_QFULL + q), 0, 3);
+                if (uo[q] > 0) wwait(bar(S::BAR_QFULL + q), (uo[q] - 1) & 1, 3);
             __syncwarp();
         } else if (warp == S::WARP_MMA) {
             // --------------------------------------------------------------
@@ -387,20 +434,28 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             // --------------------------------------------------------------
             constexpr uint32_t idesc_s = idesc_bf16_f32(BR, BC, false, false);  // Q, K both K-major
             constexpr uint32_t idesc_o = idesc_bf16_f32(BR, D, false, true);    // P (TMEM), V MN-major
-            bool ok = true;
-            for (int q = 0; q < NQ && ok; ++q)
-                if (nkv[q] > 0) ok = wwait(bar(S::BAR_QFULL + q), 0, 10);
-
             // Descriptors differ only in their start-address field (bits
             // 0..13, address >> 4): build one base per operand and add.
             const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
             const uint64_t kdesc0 = sdesc_sw128(sRing, 16, 1024);
             const uint64_t vdesc0 = sdesc_sw128(sRing, BC * 128, 1024);
-            // S_q(j) goes to S buffer j % NSB and is signalled on that buffer's barrier.
-            auto issue_s = [&](int q, int j) {
-                const int b = j & (S::NSB - 1);
+            // Running counts over all units: K/V tiles (t_base: the unit's K_0),
+            // S tiles of each query tile, and units in which each query tile ran.
+            int t_base = 0;
+            int sq[NQ], uo[NQ];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) sq[q] = uo[q] = 0;
+            auto commit = [&](int b) {
+                if (leader) tc_commit(bar(b));
+            };
+            // S_q(j) of the unit goes to S buffer (sq[q] + j) % NSB and is
+            // signalled on that buffer's barrier; after the unit's last S_q,
+            // Q_q may be reloaded.
+            auto issue_s = [&](int q, int j, int nkvq) {
+                const int b = (sq[q] + j) & (S::NSB - 1);
                 const uint64_t a0 = qdesc0 + static_cast<uint64_t>((q * S::Q_BYTES) >> 4);
-                const uint64_t b0 = kdesc0 + static_cast<uint64_t>((((2 * j) % S::NS) * S::SLOT_BYTES) >> 4);
+                const uint64_t b0 =
+                    kdesc0 + static_cast<uint64_t>((((t_base + 2 * j) % S::NS) * S::SLOT_BYTES) >> 4);
                 if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
@@ -411,13 +466,15 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                     }
                     tc_commit(bar(S::BAR_SFULL + q * S::NSB + b));
                 }
+                if (j == nkvq - 1) commit(S::BAR_QFREE + q);
             };
             // P_q V_j over K steps [BC/16 * h / NH, BC/16 * (h+1) / NH): half h of P,
             // which its warpgroup wrote over the first columns of its half of S
             constexpr int KPH = (BC / 16) / S::NH;   // K steps per half
             auto issue_pv = [&](int q, int j, int h) {
-                const int b = j & (S::NSB - 1);
-                const uint64_t b0 = vdesc0 + static_cast<uint64_t>((((2 * j + 1) % S::NS) * S::SLOT_BYTES) >> 4);
+                const int b = (sq[q] + j) & (S::NSB - 1);
+                const uint64_t b0 =
+                    vdesc0 + static_cast<uint64_t>((((t_base + 2 * j + 1) % S::NS) * S::SLOT_BYTES) >> 4);
                 if (leader) {
 #pragma unroll
                     for (int kk = (BC / 16) * h / S::NH; kk < (BC / 16) * (h + 1) / S::NH; ++kk) {
@@ -427,102 +484,133 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                     }
                 }
             };
-            auto commit = [&](int b) {
-                if (leader) tc_commit(bar(b));
+            // Before the unit's first P_q V (which overwrites O_q): the previous
+            // unit's epilogue has read O_q.  Then both halves of P_q(j).
+            auto wait_p = [&](int q, int j, int h) -> bool {
+                if (j == 0 && h == 0 && uo[q] > 0 && !wwait(bar(S::BAR_OFREE + q), (uo[q] - 1) & 1, 16))
+                    return false;
+                const int g = sq[q] + j;
+                if (!wwait(bar(S::BAR_PFULL + (q * S::NSB + (g & (S::NSB - 1))) * S::NH + h), (g / S::NSB) & 1, 13))
+                    return false;
+                tc_fence_after();
+                return true;
             };
 
-            if constexpr (S::DBS) {
-                // Two S buffers per query tile.  Order: S(0), S(1) for both
-                // tiles; then per step j: P_0 V_j, S_0(j+2), P_1 V_j, S_1(j+2).
-                // S_q(j+2) overwrites the buffer P_q(j) was read from, after it
-                // in the tensor pipe; it is ready long before the softmax wants
-                // it, so the softmax never waits for P V.
-                for (int jj = 0; ok && jj < 2 && jj < nkv_max; ++jj) {
-                    const int tk = 2 * jj;
-                    if (!wwait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, 11)) {
-                        ok = false;
-                        break;
-                    }
+            bool ok = true;
+            for (int u = 0; ok; ++u) {
+                int item, part, nparts;
+                if (!work_unit(p, cta, G, u, item, part, nparts)) break;
+                geometry(item, part, nparts);
+#pragma unroll
+                for (int q = 0; q < NQ; ++q)
+                    if (ok && nkv[q] > 0) ok = wwait(bar(S::BAR_QFULL + q), uo[q] & 1, 10);
+                if (!ok) break;
+                auto full_wait = [&](int tt, int site) -> bool {   // tile tt of the unit has landed
+                    const int tg = t_base + tt;
+                    if (!wwait(bar(S::BAR_FULL + tg % S::NS), (tg / S::NS) & 1, site)) return false;
                     tc_fence_after();
-                    for (int q = 0; q < NQ; ++q)
-                        if (jj < nkv[q]) issue_s(q, jj);
-                    commit(S::BAR_EMPTY + tk % S::NS);
-                }
-                for (int j = 0; ok && j < nkv_max; ++j) {
-                    const int tv = 2 * j + 1, tk = 2 * j + 4;
-                    if (!wwait(bar(S::BAR_FULL + tv % S::NS), (tv / S::NS) & 1, 12)) break;
-                    tc_fence_after();
-                    bool k_ready = false;
-                    for (int q = 0; q < NQ && ok; ++q) {
-                        if (j >= nkv[q]) continue;
-                        for (int h = 0; h < S::NH && ok; ++h) {
-                            if (!wwait(bar(S::BAR_PFULL + (q * S::NSB + (j & 1)) * S::NH + h), (j >> 1) & 1, 13)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            issue_pv(q, j, h);
+                    return true;
+                };
+                auto slot_of = [&](int tt) { return S::BAR_EMPTY + (t_base + tt) % S::NS; };
+
+                // The loops over q and h have compile-time bounds and no early
+                // exit, so q and h are constants after unrolling and the
+                // per-tile counts stay in registers.
+                if constexpr (S::DBS) {
+                    // Two S buffers per query tile.  Order: S(0), S(1) for both
+                    // tiles; then per step j: P_0 V_j, S_0(j+2), P_1 V_j, S_1(j+2).
+                    // S_q(j+2) overwrites the buffer P_q(j) was read from, after it
+                    // in the tensor pipe; it is ready long before the softmax wants
+                    // it, so the softmax never waits for P V.
+                    for (int jj = 0; ok && jj < 2 && jj < nkv_max; ++jj) {
+                        if (!full_wait(2 * jj, 11)) {
+                            ok = false;
+                            break;
                         }
-                        if (!ok) break;
-                        commit(S::BAR_PVDONE + q);
-                        if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
-                        if (j + 2 < nkv[q]) {
-                            if (!k_ready) {
-                                if (!wwait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, 14)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                                k_ready = true;
-                            }
-                            issue_s(q, j + 2);
-                        }
-                    }
-                    commit(S::BAR_EMPTY + tv % S::NS);               // V_j slot
-                    if (k_ready) commit(S::BAR_EMPTY + tk % S::NS);  // K_{j+2} slot
-                }
-            } else {
-                if (ok && nkv_max > 0) {
-                    ok = wwait(bar(S::BAR_FULL + 0), 0, 11);  // K_0
-                    if (ok) {
-                        tc_fence_after();
+#pragma unroll
                         for (int q = 0; q < NQ; ++q)
-                            if (nkv[q] > 0) issue_s(q, 0);
-                        commit(S::BAR_EMPTY + 0);
+                            if (jj < nkv[q]) issue_s(q, jj, nkv[q]);
+                        commit(slot_of(2 * jj));
+                    }
+                    for (int j = 0; ok && j < nkv_max; ++j) {
+                        if (!full_wait(2 * j + 1, 12)) {
+                            ok = false;
+                            break;
+                        }
+                        bool k_ready = false;
+#pragma unroll
+                        for (int q = 0; q < NQ; ++q) {
+                            if (!ok || j >= nkv[q]) continue;
+#pragma unroll
+                            for (int h = 0; h < S::NH; ++h) {
+                                if (!ok) continue;
+                                if (wait_p(q, j, h)) issue_pv(q, j, h);
+                                else ok = false;
+                            }
+                            if (!ok) continue;
+                            commit(S::BAR_PVDONE + q);
+                            if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
+                            if (j + 2 < nkv[q]) {
+                                if (!k_ready) {
+                                    if (!full_wait(2 * j + 4, 14)) {
+                                        ok = false;
+                                        continue;
+                                    }
+                                    k_ready = true;
+                                }
+                                issue_s(q, j + 2, nkv[q]);
+                            }
+                        }
+                        commit(slot_of(2 * j + 1));               // V_j slot
+                        if (k_ready) commit(slot_of(2 * j + 4));  // K_{j+2} slot
+                    }
+                } else {
+                    if (ok && nkv_max > 0) {
+                        ok = full_wait(0, 11);  // K_0
+                        if (ok) {
+#pragma unroll
+                            for (int q = 0; q < NQ; ++q)
+                                if (nkv[q] > 0) issue_s(q, 0, nkv[q]);
+                            commit(slot_of(0));
+                        }
+                    }
+                    for (int j = 0; ok && j < nkv_max; ++j) {
+                        if (!full_wait(2 * j + 1, 12)) {
+                            ok = false;
+                            break;
+                        }
+                        bool k_ready = false;
+#pragma unroll
+                        for (int q = 0; q < NQ; ++q) {
+                            if (!ok || j >= nkv[q]) continue;
+#pragma unroll
+                            for (int h = 0; h < S::NH; ++h) {
+                                if (!ok) continue;
+                                if (wait_p(q, j, h)) issue_pv(q, j, h);
+                                else ok = false;
+                            }
+                            if (!ok) continue;
+                            if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
+                            if (j + 1 < nkv[q]) {
+                                if (!k_ready) {
+                                    if (!full_wait(2 * j + 2, 14)) {
+                                        ok = false;
+                                        continue;
+                                    }
+                                    k_ready = true;
+                                }
+                                issue_s(q, j + 1, nkv[q]);
+                            }
+                        }
+                        commit(slot_of(2 * j + 1));               // V_j slot
+                        if (k_ready) commit(slot_of(2 * j + 2));  // K_{j+1} slot
                     }
                 }
-                for (int j = 0; ok && j < nkv_max; ++j) {
-                    const int tv = 2 * j + 1;
-                    if (!wwait(bar(S::BAR_FULL + tv % S::NS), (tv / S::NS) & 1, 12)) break;
-                    tc_fence_after();
-                    bool k_ready = false;
-                    const int tk = 2 * j + 2;
-                    for (int q = 0; q < NQ && ok; ++q) {
-                        if (j >= nkv[q]) continue;
-                        for (int h = 0; h < S::NH && ok; ++h) {
-                            if (!wwait(bar(S::BAR_PFULL + q * S::NH + h), j & 1, 13)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            issue_pv(q, j, h);
-                        }
-                        if (!ok) break;
-                        if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
-                        if (j + 1 < nkv[q]) {
-                            if (!k_ready) {
-                                if (!wwait(bar(S::BAR_FULL + tk % S::NS), (tk / S::NS) & 1, 14)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                                k_ready = true;
-                            }
-                            issue_s(q, j + 1);
-                        }
-                    }
-                    commit(S::BAR_EMPTY + tv % S::NS);               // V_j slot
-                    if (k_ready) commit(S::BAR_EMPTY + tk % S::NS);  // K_{j+1} slot
+                t_base += 2 * nkv_max;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    sq[q] += nkv[q];
+                    uo[q] += nkv[q] > 0 ? 1 : 0;
                 }
             }
             // Every MMA issued has completed before tensor memory is released.
@@ -541,32 +629,15 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         const int q = warp / (4 * S::NH);
         const int h = (warp >> 2) & (S::NH - 1);
         const int wq = warp & 3;
-        // This tile's row offset and K/V tile count as plain registers (a
-        // run-time index into r0[] / nkv[] would place them in local memory).
-        int r0q = r0[0], nkvq = nkv[0];
-#pragma unroll
-        for (int i = 1; i < NQ; ++i)
-            if (q == i) {
-                r0q = r0[i];
-                nkvq = nkv[i];
-            }
         // Row of this thread.  M = 128: lane l of warp w holds row 32w + l.
         // M = 64: lanes 0..15 of warp w hold rows 16w .. 16w+15.
         const bool active = (BR == 128) || (lane < 16);
         const int row_in = (BR == 128) ? wq * 32 + lane : wq * 16 + (lane & 15);
-        const int row = r0q + row_in;
         const uint32_t t_lane = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tO = tmem + t_lane + S::o_col(q);
         const float sl2 = p.scale_log2;
-        const float *mrow = MASKED ? p.key_mask + static_cast<size_t>(bh) * N : nullptr;
         constexpr int CW = BC / S::NH;       // S columns of this warpgroup
         constexpr int OC = D / 32 / S::NH;   // 32-column chunks of O of this warpgroup
-        float m = kNegInf;    // reference maximum, log2 units (the same in both warpgroups)
-        float l = 0.f;        // sum of the bf16-rounded p over this warpgroup's columns
-        // The previous tile needed its maximum and moved the reference: take
-        // this tile's maximum first instead of guessing (the same for every
-        // warp that shares the tile's rows).
-        bool max_first = false;
         bool ok = true;
         // per-row exchange slot of warpgroup hh of this tile; barrier of the pair
         auto xch = [&](int hh) -> uint32_t { return sbase + S::OFF_XCH + ((q * 2 + hh) * 128 + row_in) * 8; };
@@ -578,341 +649,127 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             pair_sync();
             asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(ao), "=f"(bo) : "r"(xch(1 - h)) : "memory");
         };
+        int sq = 0;   // S tiles of this query tile so far, all units
+        int uo = 0;   // units so far in which this query tile ran
 
-        // A wait that gives up (the error word records it; every later wait
-        // then gives up at once) does not end the loop: the tile is computed
-        // from whatever tensor memory holds, so every warp still takes part in
-        // every named barrier of the loop and no partner is left waiting.
-        for (int j = 0; j < nkvq; ++j) {
-            const int sb = j & (S::NSB - 1);   // S buffer of this tile
-            if (!mbar_wait(bar(S::BAR_SFULL + q * S::NSB + sb), (j / S::NSB) & 1, abort_flag, p.err, 20)) ok = false;
-            tc_fence_after();
-            const uint32_t tS = tmem + t_lane + S::s_col(q, sb);
-            const int key0 = kv_tile(j) * BC;
-            // block-sparse: a listed tile not marked for this query tile is masked whole
-            bool dead = false;
-            if constexpr (BSPARSE) dead = !((kv_list[j] >> (14 + q)) & 1);
-            // Tiles that need per-element masking: the N tail, the causal
-            // diagonal, or any tile when a key mask is given.
-            const bool edge = MASKED || dead || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0q);
-
-            const bool diag = p.causal && key0 + BC - 1 > r0q;   // tile crosses the causal diagonal
-            // Key mask of this warpgroup's columns, in log2 units with -inf
-            // past N; double-buffered so one barrier per tile suffices.
-            const float *msm = reinterpret_cast<const float *>(smem + S::OFF_MASK) + (q * 2 + (j & 1)) * BC;
-            if constexpr (MASKED) {
-                // Staged by all 128 threads of the warpgroup (with M = 64 two
-                // lanes share a row, so the row index would cover only half).
-                float *mw = reinterpret_cast<float *>(smem + S::OFF_MASK) + (q * 2 + (j & 1)) * BC;
+        for (int u = 0;; ++u) {
+            int item, part, nparts;
+            if (!work_unit(p, cta, G, u, item, part, nparts)) break;
+            geometry(item, part, nparts);
+            // This tile's row offset and K/V tile count as plain registers (a
+            // run-time index into r0[] / nkv[] would place them in local memory).
+            int r0q = r0[0], nkvq = nkv[0];
 #pragma unroll
-                for (int t = h * CW + wq * 32 + lane; t < (h + 1) * CW; t += 128) {
-                    const int key = key0 + t;
-                    mw[t] = (key < N) ? __ldg(mrow + key) * kLog2e : kNegInf;
+            for (int i = 1; i < NQ; ++i)
+                if (q == i) {
+                    r0q = r0[i];
+                    nkvq = nkv[i];
                 }
-                named_bar_sync(3 + q * S::NH + h, 128);
-            }
-            // One loaded 32-column chunk -> log2-domain scores
-            // x = s*scale*log2(e) (+ mask*log2(e)), -inf where not allowed.
-            auto mask_chunk = [&](int c, uint32_t *r) {
+            const int row = r0q + row_in;
+            const float *mrow = MASKED ? p.key_mask + static_cast<size_t>(bh) * N : nullptr;
+            float m = kNegInf;    // reference maximum, log2 units (the same in both warpgroups)
+            float l = 0.f;        // sum of the bf16-rounded p over this warpgroup's columns
+
+            // A wait that gives up (the error word records it; every later wait
+            // then gives up at once) does not end the loop: the tile is computed
+            // from whatever tensor memory holds, so every warp still takes part in
+            // every named barrier of the loop and no partner is left waiting.
+            for (int j = 0; j < nkvq; ++j) {
+                const int g = sq + j;              // this S tile's index over all units
+                const int sb = g & (S::NSB - 1);   // S buffer of this tile
+                if (!mbar_wait(bar(S::BAR_SFULL + q * S::NSB + sb), (g / S::NSB) & 1, abort_flag, p.err, 20)) ok = false;
+                tc_fence_after();
+                const uint32_t tS = tmem + t_lane + S::s_col(q, sb);
+                const int key0 = kv_tile(j) * BC;
+                // block-sparse: a listed tile not marked for this query tile is masked whole
+                bool dead = false;
+                if constexpr (BSPARSE) dead = !((kv_list[j] >> (14 + q)) & 1);
+                // Tiles that need per-element masking: the N tail, the causal
+                // diagonal, or any tile when a key mask is given.
+                const bool edge = MASKED || dead || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0q);
+
+                const bool diag = p.causal && key0 + BC - 1 > r0q;   // tile crosses the causal diagonal
+                // Key mask of this warpgroup's columns, in log2 units with -inf
+                // past N; double-buffered so one barrier per tile suffices.
+                const float *msm = reinterpret_cast<const float *>(smem + S::OFF_MASK) + (q * 2 + (g & 1)) * BC;
                 if constexpr (MASKED) {
-                    // four staged mask values per broadcast load, two columns per f32x2 FMA
-                    const float4 *m4 = reinterpret_cast<const float4 *>(msm + 32 * c);
-                    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                    // Staged by all 128 threads of the warpgroup (with M = 64 two
+                    // lanes share a row, so the row index would cover only half).
+                    float *mw = reinterpret_cast<float *>(smem + S::OFF_MASK) + (q * 2 + (g & 1)) * BC;
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 mv = m4[e4];
-                        float x0, x1, x2, x3;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1])), sl2x2,
-                                         f2_pack(mv.x, mv.y)), x0, x1);
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3])), sl2x2,
-                                         f2_pack(mv.z, mv.w)), x2, x3);
-                        r[4 * e4] = __float_as_uint(x0);
-                        r[4 * e4 + 1] = __float_as_uint(x1);
-                        r[4 * e4 + 2] = __float_as_uint(x2);
-                        r[4 * e4 + 3] = __float_as_uint(x3);
+                    for (int t = h * CW + wq * 32 + lane; t < (h + 1) * CW; t += 128) {
+                        const int key = key0 + t;
+                        mw[t] = (key < N) ? __ldg(mrow + key) * kLog2e : kNegInf;
                     }
+                    named_bar_sync(3 + q * S::NH + h, 128);
                 }
+                // One loaded 32-column chunk -> log2-domain scores
+                // x = s*scale*log2(e) (+ mask*log2(e)), -inf where not allowed.
+                auto mask_chunk = [&](int c, uint32_t *r) {
+                    if constexpr (MASKED) {
+                        // four staged mask values per broadcast load, two columns per f32x2 FMA
+                        const float4 *m4 = reinterpret_cast<const float4 *>(msm + 32 * c);
+                        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int key = key0 + 32 * c + e;
-                    float x = __uint_as_float(r[e]);
-                    if constexpr (!MASKED) x = (key < N) ? x * sl2 : kNegInf;
-                    if (diag) x = (key <= row) ? x : kNegInf;
-                    if constexpr (BSPARSE) x = dead ? kNegInf : x;
-                    r[e] = __float_as_uint(x);
-                }
-            };
-            auto chunk_max = [&](const uint32_t *r, float mx) {
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) mx = fmax3(mx, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-                return mx;
-            };
-            // p = 2^(x - m_use) for one chunk, packed to bf16 pairs and written
-            // over S's first BC/2 columns (chunk c -> columns 16c .. 16c+15,
-            // never ahead of the chunks still to be read).
-            // Partial sums per chunk keep the add chains short: sa / sb sum the
-            // bf16-rounded p of the even / odd columns.
-            auto exp_chunk = [&](int c, const uint32_t *r, uint64_t negm2, float &sa, float &sb) {
-                const uint64_t sl2x2 = f2_pack(sl2, sl2);
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const uint64_t xx = f2_pack(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-                    const uint64_t y = edge ? f2_add(xx, negm2) : f2_fma(xx, sl2x2, negm2);
-                    float y0, y1;
-                    f2_unpack(y, y0, y1);
-                    const float p0 = ex2(y0), p1 = ex2(y1);
-                    uint32_t w = pack_bf16x2(p0, p1);
-                    if (!active) w = 0u;
-                    pk[e] = w;
-                    add_bf16x2_f32(sa, sb, w);
-                }
-                tmem_st16(tS + 16 * c, pk);
-            };
-
-            // O_q *= alpha for this warp's rows and this warpgroup's columns
-            // (warp-collective; alpha = 1 for rows whose reference did not move).
-            auto rescale_o = [&](float alpha) {
-                const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-                for (int c = h * OC; c < (h + 1) * OC; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + 32 * c, o);
-                    tmem_ld_wait();
-                    reg_fence32(o);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
-                        float v0, v1;
-                        f2_unpack(v, v0, v1);
-                        o[e] = __float_as_uint(v0);
-                        o[e + 1] = __float_as_uint(v1);
-                    }
-                    tmem_st32(tO + 32 * c, o);
-                }
-            };
-
-            constexpr bool kTwoPass = BC > 128;   // 256 columns do not fit in registers
-            // With two S buffers the P V of tile j-1 may still run: O_q holds
-            // it only after that P V has completed.
-            auto o_settled = [&]() {
-                if constexpr (S::DBS) {
-                    mbar_wait(bar(S::BAR_PVDONE + q), (j - 1) & 1, abort_flag, p.err, 25);
-                    tc_fence_after();
-                }
-            };
-            // This warpgroup's part of P_q is in tensor memory: its P V may be issued.
-            auto release_p = [&]() {
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(bar(S::BAR_PFULL + (q * S::NSB + sb) * S::NH + h));
-            };
-            if constexpr (!kTwoPass) {
-                // This warpgroup's S columns are read from tensor memory in
-                // groups of HC; the load of the next group is in flight while
-                // one is exponentiated.
-                constexpr int HC = CW < 64 ? CW : 64;
-                constexpr int NG = CW / HC;
-                uint32_t pk[CW / 2];
-                auto issue_group = [&](int g, uint32_t *sr) {
-#pragma unroll
-                    for (int c = 0; c < HC / 32; ++c) tmem_ld32(tS + h * CW + HC * g + 32 * c, sr + 32 * c);
-                };
-                // after the wait: scale/masks where needed (EDGE: this tile needs them)
-                auto finish_group = [&](auto edge_c, int g, uint32_t *sr) {
-#pragma unroll
-                    for (int c = 0; c < HC / 32; ++c) reg_fence32(sr + 32 * c);
-                    if constexpr (decltype(edge_c)::value) {
-#pragma unroll
-                        for (int c = 0; c < HC / 32; ++c) mask_chunk((h * CW + HC * g) / 32 + c, sr + 32 * c);
-                    }
-                };
-                auto load_group = [&](auto edge_c, int g, uint32_t *sr) {
-                    issue_group(g, sr);
-                    tmem_ld_wait();
-                    finish_group(edge_c, g, sr);
-                };
-                // p = 2^(x - m_use) over this warpgroup's columns into pk (bf16
-                // pairs) and their sum; the tile's kind (edge or not) is a
-                // compile-time branch so the inner loop carries no select.
-                auto exps_k = [&](auto edge_c, float m_use, float &ls) {
-                    constexpr bool EDGE = decltype(edge_c)::value;
-                    const uint64_t negm2 = f2_pack(-m_use, -m_use);
-                    const uint64_t sl2x2 = f2_pack(sl2, sl2);
-                    ls = 0.f;
-                    uint32_t sbuf[2][HC];
-                    load_group(edge_c, 0, sbuf[0]);
-#pragma unroll
-                    for (int g = 0; g < NG; ++g) {
-                        uint32_t *sr = sbuf[g & 1];
-                        if (g + 1 < NG) issue_group(g + 1, sbuf[(g + 1) & 1]);
-#pragma unroll
-                        for (int c = 0; c < HC / 32; ++c) {
-                            float sa = 0.f, sb = 0.f;
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const float x0 = __uint_as_float(sr[32 * c + 2 * e]);
-                                const float x1 = __uint_as_float(sr[32 * c + 2 * e + 1]);
-                                const uint64_t xx = f2_pack(x0, x1);
-                                uint64_t y;
-                                if constexpr (EDGE) y = f2_add(xx, negm2);
-                                else y = f2_fma(xx, sl2x2, negm2);
-                                float y0, y1;
-                                f2_unpack(y, y0, y1);
-                                const float p0 = ex2(y0), p1 = ex2(y1);
-                                uint32_t w = pack_bf16x2(p0, p1);
-                                if (!active) w = 0u;
-                                pk[(HC / 2) * g + 16 * c + e] = w;
-                                add_bf16x2_f32(sa, sb, w);
-                            }
-                            ls += sa + sb;
-                        }
-                        if (g + 1 < NG) {
-                            tmem_ld_wait();
-                            finish_group(edge_c, g + 1, sbuf[(g + 1) & 1]);
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 mv = m4[e4];
+                            float x0, x1, x2, x3;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1])), sl2x2,
+                                             f2_pack(mv.x, mv.y)), x0, x1);
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3])), sl2x2,
+                                             f2_pack(mv.z, mv.w)), x2, x3);
+                            r[4 * e4] = __float_as_uint(x0);
+                            r[4 * e4 + 1] = __float_as_uint(x1);
+                            r[4 * e4 + 2] = __float_as_uint(x2);
+                            r[4 * e4 + 3] = __float_as_uint(x3);
                         }
                     }
-                };
-                auto exps = [&](float m_use, float &ls) {
-                    if (edge) exps_k(std::true_type{}, m_use, ls);
-                    else exps_k(std::false_type{}, m_use, ls);
-                };
-                // P chunk c (32 keys) of this warpgroup -> its S columns 16c .. 16c+15
-                auto store_p = [&]() {
 #pragma unroll
-                    for (int c = 0; c < CW / 32; ++c) tmem_st16(tS + h * CW + 16 * c, pk + 16 * c);
-                };
-                // maximum over this warpgroup's columns, 32 at a time (log2 units)
-                auto cols_max = [&]() {
-                    float mx = kNegInf;
-#pragma unroll
-                    for (int c = 0; c < CW / 32; ++c) {
-                        uint32_t sr[32];
-                        tmem_ld32(tS + h * CW + 32 * c, sr);
-                        tmem_ld_wait();
-                        reg_fence32(sr);
-                        mask_chunk(h * CW / 32 + c, sr);
-                        mx = chunk_max(sr, mx);
+                    for (int e = 0; e < 32; ++e) {
+                        const int key = key0 + 32 * c + e;
+                        float x = __uint_as_float(r[e]);
+                        if constexpr (!MASKED) x = (key < N) ? x * sl2 : kNegInf;
+                        if (diag) x = (key <= row) ? x : kNegInf;
+                        if constexpr (BSPARSE) x = dead ? kNegInf : x;
+                        r[e] = __float_as_uint(x);
                     }
+                };
+                auto chunk_max = [&](const uint32_t *r, float mx) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) mx = fmax3(mx, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
                     return mx;
                 };
-                // Guess: exponentiate against the current reference with no
-                // maximum.  A row whose sum exceeds kFastSumLimit (or
-                // overflows, or has no finite reference yet) has a score far
-                // past the reference: only then is the tile's maximum taken,
-                // the reference moved and the tile redone (S is still intact:
-                // P is written after).  The first tile of a row, and a tile
-                // after one that moved the reference, take the maximum first.
-                // Either way the reference moves only to a maximum more than
-                // kRescaleThresh above it, so every p stays below 2^16.
-                const bool guess = j > 0 && !max_first;
-                float ls = 0.f;
-                bool redo = true;
-                if (guess) {
-                    exps(m, ls);
-                    const bool need = active && !(ls <= kFastSumLimit);
-                    if constexpr (S::NH == 2) redo = named_bar_red_or(7 + q, 256, need);
-                    else redo = __any_sync(0xffffffffu, need);
-                }
-                if (redo) {
-                    float mx = cols_max();
-                    if constexpr (S::NH == 2) {
-                        float mo, unused;
-                        exchange(mx, 0.f, mo, unused);
-                        mx = fmaxf(mx, mo);
-                    }
-                    // (m = -inf: any finite maximum is taken; nothing to scale)
-                    const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
-                    const bool moved = m_new != m;
-                    const float a = moved ? ex2(m - m_new) : 1.f;
-                    if (j > 0 && __any_sync(0xffffffffu, moved)) {
-                        o_settled();
-                        rescale_o(a);
-                    }
-                    // (the first tile's move from -inf says nothing about the next)
-                    if constexpr (S::NH == 2) max_first = named_bar_red_or(7 + q, 256, j > 0 && moved);
-                    else max_first = __any_sync(0xffffffffu, j > 0 && moved);
-                    m = m_new;
-                    l *= a;
-                    exps(m == kNegInf ? 0.f : m, ls);
-                    // P is stored in each branch: a shared store after the
-                    // branch would keep the first pass's P live through this one
-                    l += ls;
-                    store_p();
-                    release_p();
-                } else {
-                    l += ls;
-                    store_p();
-                    release_p();
-                }
-            } else {
-                float tile_ls = 0.f;
-                uint32_t sr[32];
-                float mx = kNegInf;
-#pragma unroll 1
-                for (int c = 0; c < BC / 32; ++c) {
-                    tmem_ld32(tS + 32 * c, sr);
-                    tmem_ld_wait();
-                    reg_fence32(sr);
-                    if (edge) mask_chunk(c, sr);
-                    mx = chunk_max(sr, mx);
-                }
-                if (!edge) mx *= sl2;
-                const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
-                const bool moved = (m_new != m);
-                const float alpha = moved ? ex2(m - m_new) : 1.f;
-                const float m_use = (m_new == kNegInf) ? 0.f : m_new;
-                if (j > 0 && __any_sync(0xffffffffu, moved)) {
-                    o_settled();
-                    rescale_o(alpha);
-                }
-                m = m_new;
-                const uint64_t negm2 = f2_pack(-m_use, -m_use);
-#pragma unroll 1
-                for (int c = 0; c < BC / 32; ++c) {
-                    tmem_ld32(tS + 32 * c, sr);
-                    tmem_ld_wait();
-                    reg_fence32(sr);
-                    if (edge) mask_chunk(c, sr);
-                    float sa = 0.f, sb = 0.f;
-                    exp_chunk(c, sr, negm2, sa, sb);
-                    tile_ls += sa + sb;
-                }
-                l = l * alpha + tile_ls;
-                release_p();
-            }
-        }
-
-        // ---------------- epilogue ----------------
-        // Two warpgroups per tile: each row's sum over all columns.
-        if constexpr (S::NH == 2) {
-            float lo, unused;
-            pair_sync();   // the other warpgroup has read the last tile's exchange
-            exchange(l, 0.f, lo, unused);
-            l += lo;
-        }
-        // A split item: every part but the first publishes its partial result
-        // (unnormalised O, m, l per row) in its own shared
-        // memory; the first part merges them with its own, with the same
-        // rescale as between tiles: M = max_p m_p, weights 2^(m_p - M).
-        if (nkvq > 0 && ok) ok = mbar_wait(bar(S::BAR_OFULL + q), 0, abort_flag, p.err, 21);
-        tc_fence_after();
-        float a_own = 1.f;                 // weight of this CTA's O
-        float a_part[8];                   // weights of the other parts' O
-        float l_fin = l, m_fin = m;
-        bool write_out = true;
-        const uint32_t sPart = sQ;         // partials live in the (now idle) Q tiles and K/V ring
-        const uint32_t part_row = sPart + ((q * 128 + row_in) * S::PSTR) * 4;
-        auto stat_addr = [&](int k) { return sPart + (NQ * 128 * S::PSTR + k * NQ * 128 + q * 128 + row_in) * 4; };
+                // p = 2^(x - m_use) for one 32-column chunk, packed to bf16 pairs
+                // and written to the 16 columns from pcol.  EDGE: the chunk is
+                // already scaled and masked (a compile-time branch, so the
+                // inner loop carries no select).
+                // Partial sums per chunk keep the add chains short: sa / sb sum the
+                // bf16-rounded p of the even / odd columns.
+                auto exp_chunk = [&](auto edge_c, int pcol, const uint32_t *r, uint64_t negm2, float &sa, float &sb) {
+                    constexpr bool EDGE = decltype(edge_c)::value;
+                    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                    uint32_t pk[16];
 #pragma unroll
-        for (int pp = 0; pp < 8; ++pp) a_part[pp] = 0.f;
-        if constexpr (S::CAN_SPLIT) {
-            if (nparts > 1 && part > 0) {
-                // The ring is reused only after every MMA of the CTA (both query
-                // tiles) has completed: the other tile's last PV may still read V.
-                mbar_wait(bar(S::BAR_DONE), 0, abort_flag, p.err, 24);
-                tc_fence_after();
-                if (nkvq > 0) {
+                    for (int e = 0; e < 16; ++e) {
+                        const uint64_t xx = f2_pack(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                        uint64_t y;
+                        if constexpr (EDGE) y = f2_add(xx, negm2);
+                        else y = f2_fma(xx, sl2x2, negm2);
+                        float y0, y1;
+                        f2_unpack(y, y0, y1);
+                        const float p0 = ex2(y0), p1 = ex2(y1);
+                        uint32_t w = pack_bf16x2(p0, p1);
+                        if (!active) w = 0u;
+                        pk[e] = w;
+                        add_bf16x2_f32(sa, sb, w);
+                    }
+                    tmem_st16(tS + pcol, pk);
+                };
+
+                // O_q *= alpha for this warp's rows and this warpgroup's columns
+                // (warp-collective; alpha = 1 for rows whose reference did not move).
+                auto rescale_o = [&](float alpha) {
+                    const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
                     for (int c = h * OC; c < (h + 1) * OC; ++c) {
                         uint32_t o[32];
@@ -920,121 +777,306 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                         tmem_ld_wait();
                         reg_fence32(o);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(part_row + (32 * c + 4 * k) * 4),
-                                         "r"(o[4 * k]), "r"(o[4 * k + 1]), "r"(o[4 * k + 2]), "r"(o[4 * k + 3])
-                                         : "memory");
+                        for (int e = 0; e < 32; e += 2) {
+                            const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+                            float v0, v1;
+                            f2_unpack(v, v0, v1);
+                            o[e] = __float_as_uint(v0);
+                            o[e + 1] = __float_as_uint(v1);
+                        }
+                        tmem_st32(tO + 32 * c, o);
                     }
-                }
-                if (h == 0) {
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(0)), "f"(m) : "memory");
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(1)), "f"(l) : "memory");
-                }
-                mbar_arrive_remote(mapa_shared(bar(S::BAR_PART), 0));
-                // This CTA's shared memory outlives the first part's reads: every
-                // thread of every part meets at the cluster barrier at the end.
-                write_out = false;
-            } else if (nparts > 1) {
-                // A failed wait (the error word has it) reads no partial: the
-                // merge then has only this part's keys, and the O / LSE stores
-                // below are skipped because the abort flag is set.
-                const bool parts_ok = mbar_wait_cluster(bar(S::BAR_PART), 0, abort_flag, p.err, 23);
-                float mp[8], lp[8];
-                m_fin = m;
+                };
+
+                // With two S buffers the P V of tile j-1 may still run: O_q holds
+                // it only after that P V has completed.
+                auto o_settled = [&]() {
+                    if constexpr (S::DBS) {
+                        mbar_wait(bar(S::BAR_PVDONE + q), (g - 1) & 1, abort_flag, p.err, 25);
+                        tc_fence_after();
+                    }
+                };
+                // This warpgroup's part of P_q is in tensor memory: its P V may be issued.
+                auto release_p = [&]() {
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(bar(S::BAR_PFULL + (q * S::NSB + sb) * S::NH + h));
+                };
+                constexpr int NC = CW / 32;   // 32-column chunks of this warpgroup
+                if constexpr (NC <= 2) {
+                    // One pass: this warpgroup's S columns stay in registers.
+                    // The tile's row maximum comes with the loads (interior
+                    // tiles) or after masking (edge tiles); two warpgroups
+                    // exchange theirs.
+                    uint32_t sr[NC][32];
+                    float mxc[NC];
+                    float mx = kNegInf;
 #pragma unroll
-                for (int pp = 1; pp < 8; ++pp) {
-                    if (pp >= nparts) break;
-                    mp[pp] = kNegInf;
-                    lp[pp] = 0.f;
-                    if (parts_ok) {
-                        mp[pp] = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
-                        lp[pp] = ld_cluster_f32(mapa_shared(stat_addr(1), pp));
+                    for (int c = 0; c < NC; ++c) {
+                        if (edge) tmem_ld32(tS + h * CW + 32 * c, sr[c]);
+                        else tmem_ld32_max(tS + h * CW + 32 * c, sr[c], mxc[c]);
                     }
-                    m_fin = fmaxf(m_fin, mp[pp]);
-                }
-                if (m_fin == kNegInf) {
-                    a_own = 0.f;
-                    l_fin = 0.f;
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        reg_fence32(sr[c]);
+                        if (edge) {
+                            mask_chunk(h * NC + c, sr[c]);
+                            mx = chunk_max(sr[c], mx);
+                        } else {
+                            mx = fmaxf(mx, mxc[c]);
+                        }
+                    }
+                    if (!edge) mx *= sl2;
+                    if constexpr (S::NH == 2) {
+                        // The row maximum over both halves is needed only if some
+                        // row's half maximum would move the reference: one vote,
+                        // and the exchange only then.
+                        if (named_bar_red_or(7 + q, 256, active && mx > m + kRescaleThresh)) {
+                            float mo, unused;
+                            exchange(mx, 0.f, mo, unused);
+                            mx = fmaxf(mx, mo);
+                        } else {
+                            mx = m;
+                        }
+                    }
+                    // The reference moves only to a maximum more than
+                    // kRescaleThresh above it (from -inf: to any finite
+                    // maximum), so every p stays below 2^kRescaleThresh and O
+                    // is rescaled only then.
+                    const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
+                    const bool moved = m_new != m;
+                    const float a = moved ? ex2(m - m_new) : 1.f;
+                    m = m_new;
+                    const float m_use = (m == kNegInf) ? 0.f : m;
+                    const uint64_t negm2 = f2_pack(-m_use, -m_use);
+                    // P chunk c goes over this half's columns 16c .. 16c+15,
+                    // already read into registers.
+                    float ls = 0.f;
+                    auto exps = [&](auto edge_c) {
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) {
+                            float sa = 0.f, sb = 0.f;
+                            exp_chunk(edge_c, h * CW + 16 * c, sr[c], negm2, sa, sb);
+                            ls += sa + sb;
+                        }
+                    };
+                    if (edge) exps(std::true_type{});
+                    else exps(std::false_type{});
+                    // O_q takes the new reference before this tile's P V
+                    // accumulates into it (S is no longer held).
+                    if (j > 0 && __any_sync(0xffffffffu, moved)) {
+                        o_settled();
+                        rescale_o(a);
+                    }
+                    l = l * a + ls;
+                    release_p();
                 } else {
-                    a_own = (m == kNegInf) ? 0.f : ex2(m - m_fin);
-                    l_fin = a_own * l;
-#pragma unroll
-                    for (int pp = 1; pp < 8; ++pp) {
-                        if (pp >= nparts) break;
-                        a_part[pp] = (mp[pp] == kNegInf) ? 0.f : ex2(mp[pp] - m_fin);
-                        l_fin += a_part[pp] * lp[pp];
+                    // Two passes (the columns do not fit in registers): the
+                    // row maximum first, then the exponentials.
+                    float mx = kNegInf;
+#pragma unroll 1
+                    for (int c = 0; c < NC; ++c) {
+                        uint32_t sr[32];
+                        float mc;
+                        if (edge) {
+                            tmem_ld32(tS + h * CW + 32 * c, sr);
+                            tmem_ld_wait();
+                            reg_fence32(sr);
+                            mask_chunk(h * NC + c, sr);
+                            mx = chunk_max(sr, mx);
+                        } else {
+                            tmem_ld32_max(tS + h * CW + 32 * c, sr, mc);
+                            tmem_ld_wait();
+                            reg_fence32(sr);
+                            mx = fmaxf(mx, mc);
+                        }
                     }
+                    if (!edge) mx *= sl2;
+                    if constexpr (S::NH == 2) {
+                        float mo, unused;
+                        exchange(mx, 0.f, mo, unused);
+                        mx = fmaxf(mx, mo);
+                    }
+                    const float m_new = (active && mx > m + kRescaleThresh) ? mx : m;
+                    const bool moved = m_new != m;
+                    const float a = moved ? ex2(m - m_new) : 1.f;
+                    if (j > 0 && __any_sync(0xffffffffu, moved)) {
+                        o_settled();
+                        rescale_o(a);
+                    }
+                    m = m_new;
+                    l *= a;
+                    const float m_use = (m == kNegInf) ? 0.f : m;
+                    const uint64_t negm2 = f2_pack(-m_use, -m_use);
+                    // P chunk c goes over this half's columns 16c .. 16c+15,
+                    // never ahead of the columns still to be read.
+                    float ls = 0.f;
+                    uint32_t sr[2][32];
+                    tmem_ld32(tS + h * CW, sr[0]);
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        tmem_ld_wait();
+                        reg_fence32(sr[c & 1]);
+                        if (c + 1 < NC) tmem_ld32(tS + h * CW + 32 * (c + 1), sr[(c + 1) & 1]);
+                        if (edge) mask_chunk(h * NC + c, sr[c & 1]);
+                        float sa = 0.f, sb = 0.f;
+                        if (edge) exp_chunk(std::true_type{}, h * CW + 16 * c, sr[c & 1], negm2, sa, sb);
+                        else exp_chunk(std::false_type{}, h * CW + 16 * c, sr[c & 1], negm2, sa, sb);
+                        ls += sa + sb;
+                    }
+                    l += ls;
+                    release_p();
                 }
             }
-        }
-        if (nkvq > 0 && write_out) {
-            const bool any = l_fin > 0.f;
-            const float inv = any ? 1.f / l_fin : 0.f;
-            const uint64_t inv2 = f2_pack(inv, inv);
-            const uint32_t stage = sQ + q * S::Q_BYTES;  // Q_q is no longer read
+
+            // ---------------- epilogue ----------------
+            // Two warpgroups per tile: each row's sum over all columns.
+            if constexpr (S::NH == 2) {
+                float lo, unused;
+                pair_sync();   // the other warpgroup has read the last tile's exchange
+                exchange(l, 0.f, lo, unused);
+                l += lo;
+                pair_sync();   // both have read it: the next unit may exchange again
+            }
+            // A split item: every part but the first publishes its partial result
+            // (unnormalised O, m, l per row) in its own shared
+            // memory; the first part merges them with its own, with the same
+            // rescale as between tiles: M = max_p m_p, weights 2^(m_p - M).
+            if (nkvq > 0 && ok) ok = mbar_wait(bar(S::BAR_OFULL + q), uo & 1, abort_flag, p.err, 21);
+            tc_fence_after();
+            float a_own = 1.f;                 // weight of this CTA's O
+            float l_fin = l, m_fin = m;
+            bool parts_ok = false;             // the other parts' partials may be read
+            bool write_out = true;
+            const uint32_t sPart = sQ;         // partials live in the (now idle) Q tiles and K/V ring
+            const uint32_t part_row = sPart + ((q * 128 + row_in) * S::PSTR) * 4;
+            auto stat_addr = [&](int k) { return sPart + (NQ * 128 * S::PSTR + k * NQ * 128 + q * 128 + row_in) * 4; };
+            if constexpr (S::CAN_SPLIT) {
+                if (nparts > 1 && part > 0) {
+                    // The ring is reused only after every MMA of the CTA (both query
+                    // tiles) has completed: the other tile's last PV may still read V.
+                    mbar_wait(bar(S::BAR_DONE), 0, abort_flag, p.err, 24);
+                    tc_fence_after();
+                    if (nkvq > 0) {
 #pragma unroll
-            for (int c = h * OC; c < (h + 1) * OC; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + 32 * c, o);
-                tmem_ld_wait();
-                reg_fence32(o);
-                if constexpr (S::CAN_SPLIT) {
-                    if (nparts > 1) {
-                        // O = a_own O_own + sum_p a_p O_p (other parts read from
-                        // their shared memory through the cluster)
+                        for (int c = h * OC; c < (h + 1) * OC; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + 32 * c, o);
+                            tmem_ld_wait();
+                            reg_fence32(o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a_own);
-#pragma unroll
-                        for (int pp = 1; pp < 8; ++pp) {
-                            if (pp >= nparts) break;
-                            if (a_part[pp] == 0.f) continue;
-                            const uint32_t src = mapa_shared(part_row + 32 * c * 4, pp);
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                float v0, v1, v2, v3;
-                                ld_cluster_v4(src + 16 * k, v0, v1, v2, v3);
-                                o[4 * k] = __float_as_uint(fmaf(a_part[pp], v0, __uint_as_float(o[4 * k])));
-                                o[4 * k + 1] = __float_as_uint(fmaf(a_part[pp], v1, __uint_as_float(o[4 * k + 1])));
-                                o[4 * k + 2] = __float_as_uint(fmaf(a_part[pp], v2, __uint_as_float(o[4 * k + 2])));
-                                o[4 * k + 3] = __float_as_uint(fmaf(a_part[pp], v3, __uint_as_float(o[4 * k + 3])));
-                            }
+                            for (int k = 0; k < 8; ++k)
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(part_row + (32 * c + 4 * k) * 4),
+                                             "r"(o[4 * k]), "r"(o[4 * k + 1]), "r"(o[4 * k + 2]), "r"(o[4 * k + 3])
+                                             : "memory");
+                        }
+                    }
+                    if (h == 0) {
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(0)), "f"(m) : "memory");
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(1)), "f"(l) : "memory");
+                    }
+                    mbar_arrive_remote(mapa_shared(bar(S::BAR_PART), 0));
+                    // This CTA's shared memory outlives the first part's reads: every
+                    // thread of every part meets at the cluster barrier at the end.
+                    write_out = false;
+                } else if (nparts > 1) {
+                    // A failed wait (the error word has it) reads no partial: the
+                    // merge then has only this part's keys, and the O / LSE stores
+                    // below are skipped because the abort flag is set.
+                    // (the parts' statistics are read again where needed rather
+                    // than held in registers)
+                    parts_ok = mbar_wait_cluster(bar(S::BAR_PART), 0, abort_flag, p.err, 23);
+                    m_fin = m;
+                    for (int pp = 1; parts_ok && pp < nparts; ++pp)
+                        m_fin = fmaxf(m_fin, ld_cluster_f32(mapa_shared(stat_addr(0), pp)));
+                    if (m_fin == kNegInf) {
+                        a_own = 0.f;
+                        l_fin = 0.f;
+                    } else {
+                        a_own = (m == kNegInf) ? 0.f : ex2(m - m_fin);
+                        l_fin = a_own * l;
+                        for (int pp = 1; parts_ok && pp < nparts; ++pp) {
+                            const float mp = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
+                            if (mp != kNegInf) l_fin += ex2(mp - m_fin) * ld_cluster_f32(mapa_shared(stat_addr(1), pp));
                         }
                     }
                 }
-                uint32_t w[16];
+            }
+            if (nkvq > 0 && write_out) {
+                const bool any = l_fin > 0.f;
+                const float inv = any ? 1.f / l_fin : 0.f;
+                const uint64_t inv2 = f2_pack(inv, inv);
+                // this thread's row of O, 64 bytes per 32-column chunk: two
+                // 32-byte stores (whole sectors) when O is 32-byte aligned
+                const bool store = active && row < N && !*abort_flag;
+                const bool wide = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
+                __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * N + (store ? row : 0)) * D;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2);
-                    float v0, v1;
-                    f2_unpack(v, v0, v1);
-                    w[e] = pack_bf16x2(v0, v1);
-                }
-                if (active) {
-                    const int cb = c >> 1;
+                for (int c = h * OC; c < (h + 1) * OC; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32 * c, o);
+                    tmem_ld_wait();
+                    reg_fence32(o);
+                    if constexpr (S::CAN_SPLIT) {
+                        if (nparts > 1) {
+                            // O = a_own O_own + sum_p a_p O_p (other parts read from
+                            // their shared memory through the cluster)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int ch = (c & 1) * 4 + k;  // 16-byte chunk within the 128-byte row
-                        const uint32_t addr =
-                            stage + cb * (BR * 128) + row_in * 128 + ((ch ^ (row_in & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * k]),
-                                     "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
-                                     : "memory");
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a_own);
+                            for (int pp = 1; parts_ok && pp < nparts; ++pp) {
+                                const float mp = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
+                                if (mp == kNegInf || m_fin == kNegInf) continue;
+                                const float ap = ex2(mp - m_fin);
+                                const uint32_t src = mapa_shared(part_row + 32 * c * 4, pp);
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) {
+                                    float v0, v1, v2, v3;
+                                    ld_cluster_v4(src + 16 * k, v0, v1, v2, v3);
+                                    o[4 * k] = __float_as_uint(fmaf(ap, v0, __uint_as_float(o[4 * k])));
+                                    o[4 * k + 1] = __float_as_uint(fmaf(ap, v1, __uint_as_float(o[4 * k + 1])));
+                                    o[4 * k + 2] = __float_as_uint(fmaf(ap, v2, __uint_as_float(o[4 * k + 2])));
+                                    o[4 * k + 3] = __float_as_uint(fmaf(ap, v3, __uint_as_float(o[4 * k + 3])));
+                                }
+                            }
+                        }
+                    }
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2);
+                        float v0, v1;
+                        f2_unpack(v, v0, v1);
+                        w[e] = pack_bf16x2(v0, v1);
+                    }
+                    if (store && wide) {
+#pragma unroll
+                        for (int k = 0; k < 2; ++k)
+                            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
+                                             orow + 32 * c + 16 * k),
+                                         "r"(w[8 * k]), "r"(w[8 * k + 1]), "r"(w[8 * k + 2]), "r"(w[8 * k + 3]),
+                                         "r"(w[8 * k + 4]), "r"(w[8 * k + 5]), "r"(w[8 * k + 6]), "r"(w[8 * k + 7])
+                                         : "memory");
+                    } else if (store) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(orow + 32 * c + 8 * k),
+                                         "r"(w[4 * k]), "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
+                                         : "memory");
                     }
                 }
+                if (h == 0 && active && p.lse != nullptr && row < N && !*abort_flag) {
+                    p.lse[static_cast<size_t>(bh) * N + row] = any ? (m_fin + log2f(l_fin)) * kLn2 : kNegInf;
+                }
             }
-            fence_proxy_async_smem();
-            named_bar_sync(1 + q, 128 * S::NH);
-            if (h == 0 && wq == 0 && lane == 0 && !*abort_flag) {
-#pragma unroll
-                for (int cb = 0; cb < S::CB; ++cb)
-                    tma_store_3d(&tm_o, stage + cb * (BR * 128), cb * 64, r0q, bh);
-                tma_store_commit();
-                tma_store_wait_read0();
+            if (nkvq > 0) {
+                // The epilogue has read O_q: the next unit's first P V may overwrite it.
+                tc_fence_before();
+                mbar_arrive(bar(S::BAR_OFREE + q));
             }
-            if (h == 0 && active && p.lse != nullptr && row < N && !*abort_flag) {
-                p.lse[static_cast<size_t>(bh) * N + row] = any ? (m_fin + log2f(l_fin)) * kLn2 : kNegInf;
-            }
-        }
+            sq += nkvq;
+            uo += nkvq > 0 ? 1 : 0;
+        }   // work units
     }
 
     tc_fence_before();
@@ -1047,19 +1089,22 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         // Split item: no part exits while the first part may still read its
         // shared memory.  Every thread reaches this point on every path (all
         // waits above are bounded), so the barrier always completes.
-        if (nparts > 1) cluster_sync();
+        if (p.split > 1) cluster_sync();
     }
 }
 
+constexpr int kMaxDev = 64;
+std::mutex g_launch_mu;   // serialises the once-per-device set-up below
+
 int sm_count(int dev) {
-    static int counts[64];
-    if (dev < 0 || dev >= 64) return 0;
-    if (counts[dev] == 0) {
-        int n = 0;
+    static std::atomic<int> counts[kMaxDev];
+    if (dev < 0 || dev >= kMaxDev) return 0;
+    int n = counts[dev].load(std::memory_order_acquire);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        counts[dev] = n;
+        counts[dev].store(n, std::memory_order_release);
     }
-    return counts[dev];
+    return n;
 }
 
 template <int D, int BR, int BC, int NQ, bool MASKED, bool BSPARSE = false>
@@ -1068,24 +1113,50 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
                    const uint8_t *block_mask = nullptr) {
     using S = TcShape<D, BR, BC, NQ, MASKED, BSPARSE>;
     auto kern = attn_fwd_tc_kernel<D, BR, BC, NQ, MASKED, BSPARSE>;
-    static int attr_device = -1;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
-    if (attr_device != dev) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES) != cudaSuccess)
-            return kErrCuda;
-        if (S::MOVE_REGS) {
-            // setmaxnreg moves registers within the launch allocation; the split
-            // above is exact only for this per-thread count.
-            cudaFuncAttributes fa;
-            if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return kErrCuda;
-            if (fa.numRegs != S::LAUNCH_REGS) return kErrUnsupported;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return kErrCuda;
+    // Once per device: the shared-memory opt-in, and how many clusters of 2,
+    // 4 and 8 CTAs can be resident at once (a split tail is used only if
+    // every cluster of it fits in one wave).
+    static std::atomic<int> ready[kMaxDev];
+    static int max_clusters[kMaxDev][4];
+    if (ready[dev].load(std::memory_order_acquire) == 0) {
+        std::lock_guard<std::mutex> lk(g_launch_mu);
+        if (ready[dev].load(std::memory_order_relaxed) == 0) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES) != cudaSuccess)
+                return kErrCuda;
+            if (S::MOVE_REGS) {
+                // setmaxnreg moves registers within the launch allocation; the split
+                // above is exact only for this per-thread count.
+                cudaFuncAttributes fa;
+                if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return kErrCuda;
+                if (fa.numRegs != S::LAUNCH_REGS) return kErrUnsupported;
+            }
+            for (int i = 1; i < 4; ++i) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(8u);
+                cfg.blockDim = dim3(S::THREADS);
+                cfg.dynamicSmemBytes = S::SMEM_BYTES;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 1u << i;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    n = 0;
+                }
+                max_clusters[dev][i] = n;
+            }
+            ready[dev].store(1, std::memory_order_release);
         }
-        attr_device = dev;
     }
-    CUtensorMap tq, tk, tv, to;
-    if (!make_bf16_rows_map(&tq, Q, D, N, BH, BR) || !make_bf16_rows_map(&tk, K, D, N, BH, BC) || !make_bf16_rows_map(&tv, V, D, N, BH, BC) ||
-        !make_bf16_rows_map(&to, O, D, N, BH, BR))
+    CUtensorMap tq, tk, tv;
+    if (!make_bf16_rows_map(&tq, Q, D, N, BH, BR) || !make_bf16_rows_map(&tk, K, D, N, BH, BC) ||
+        !make_bf16_rows_map(&tv, V, D, N, BH, BC))
         return kErrCuda;
     TcParams p;
     p.N = N;
@@ -1096,31 +1167,39 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
     p.key_mask = key_mask;
     p.block_mask = block_mask;
     p.nkb = (N + 127) / 128;
+    p.o = static_cast<__nv_bfloat16 *>(O);
     p.lse = LSE;
     p.err = device_error_word();
     if (!p.err) return kErrCuda;
-    // One CTA per SM: the items beyond the last full wave are split along K/V
-    // into s parts (a cluster of s CTAs each) so that the tail wave is as
-    // short as the SMs allow.  Causal work is uneven and stays unsplit.
     const long long items = static_cast<long long>(p.num_qg) * BH;
     if (items > 0x7fffffffLL) return kErrUnsupported;
-    int split = 1;
-    long long n_full = items;
     const int nsm = sm_count(dev);
-    if (S::CAN_SPLIT && !causal && nsm > 0) {
+    if (nsm <= 0) return kErrCuda;
+    // Work: one CTA per SM, each running a list of work units (TcParams).
+    // Non-causal items past the last full round are split along K/V into s
+    // parts, s the largest power of two with s * (items mod SMs) <= SMs, run
+    // by clusters of s CTAs; causal work is uneven and stays unsplit.  The
+    // block-sparse variant runs one CTA per item.
+    long long grid = BSPARSE ? items : std::min<long long>(items, nsm);
+    long long n_full = items;
+    int split = 1;
+    if (S::CAN_SPLIT && !causal) {
         const long long R = items % nsm;
         const int nkv_all = (N + BC - 1) / BC;
         int sp = 1;
-        while (R > 0 && sp * 2 <= 8 && sp * 2 * R <= nsm && sp * 2 <= nkv_all) sp *= 2;
-        if (sp > 1 && (items - R) % sp == 0) {
+        while (R > 0 && sp * 2 <= 8 && sp * 2 * R <= nsm && sp * 2 <= nkv_all && nsm % (sp * 2) == 0) sp *= 2;
+        const int si = sp == 8 ? 3 : sp == 4 ? 2 : sp == 2 ? 1 : 0;
+        const long long g = (items - R > 0) ? nsm : R * sp;
+        if (sp > 1 && static_cast<long long>(max_clusters[dev][si]) * sp >= g) {
             split = sp;
             n_full = items - R;
+            grid = g;
         }
     }
+    p.items = static_cast<int>(items);
     p.n_full = static_cast<int>(n_full);
     p.split = split;
-    const long long grid = n_full + (items - n_full) * split;
-    if (grid > 0x7fffffffLL) return kErrUnsupported;
+    p.split_shift = split == 8 ? 3 : split == 4 ? 2 : split == 2 ? 1 : 0;
     if (split > 1) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -1134,16 +1213,18 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, p) == cudaSuccess) {
+        if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p) == cudaSuccess) {
             if (split_out) *split_out = split;
             return kOk;
         }
         (void)cudaGetLastError();   // cluster not schedulable: run unsplit
-        p.n_full = static_cast<int>(items);
+        p.n_full = p.items;
         p.split = 1;
+        p.split_shift = 0;
+        grid = BSPARSE ? items : std::min<long long>(items, nsm);
     }
     if (split_out) *split_out = 1;
-    kern<<<static_cast<unsigned>(items), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
+    kern<<<static_cast<unsigned>(grid), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 

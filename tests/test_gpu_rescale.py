@@ -125,10 +125,12 @@ def test_adversarial_logits_every_variant(eta, d, Br, Bc, causal):
     assert f"_br{Br}_bc{Bc}_" in eta.attn_last_variant()
 
 
-def _heads_for_split(nsm, num_qg, split, nkv):
-    """Heads H (B = 1) whose launch ends in a tail wave that the launcher splits
-    into `split` parts: items = H * num_qg = k * nsm + R with split * R <= nsm
-    and (for split < 8) 2 * split * R > nsm."""
+def _heads_for_split(nsm, num_qg, split, nkv, after_full_rounds):
+    """Heads H (B = 1) whose items (H * num_qg of them) leave R = items mod nsm
+    past the last full round with split * R <= nsm and, below 8 parts,
+    2 * split * R > nsm: the launcher then splits each of those R items into
+    `split` parts.  after_full_rounds: items = nsm + R (a full round of whole
+    items first), else items = R (the launch is the split tail alone)."""
     if nsm % split or split > nkv:
         return None
     for R in range(1, nsm + 1):
@@ -136,26 +138,28 @@ def _heads_for_split(nsm, num_qg, split, nkv):
             break
         if split < 8 and 2 * split * R <= nsm:
             continue
-        if (nsm + R) % num_qg == 0:
-            return (nsm + R) // num_qg
+        items = nsm + R if after_full_rounds else R
+        if items % num_qg == 0:
+            return items // num_qg
     return None
 
 
-@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("split,after_full_rounds", [(2, True), (2, False), (4, False), (8, False)])
 @pytest.mark.parametrize("d,Bc", [(128, 128), (64, 128), (128, 64), (64, 256)])
-def test_adversarial_logits_split_tail(eta, d, Bc, split):
-    """Non-causal items past the last full wave are split along K/V over the
+def test_adversarial_logits_split_tail(eta, d, Bc, split, after_full_rounds):
+    """Non-causal items past the last full round are split along K/V over the
     CTAs of a cluster and merged with the tiles' rescale rule.  Heads are
-    chosen from the SM count so that the tail splits into 2, 4 or 8 parts;
-    one head has every key masked (each part's maximum is -inf)."""
+    chosen from the SM count so that the tail splits into 2, 4 or 8 parts,
+    after a full round of whole items or as the whole launch; one head has
+    every key masked (each part's maximum is -inf)."""
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     N, Br = 1000, 128
     nq = 2 if 2 * (Bc + d) <= 512 else 1
     num_qg = -(-N // (nq * Br))
-    H = _heads_for_split(nsm, num_qg, split, -(-N // Bc))
+    H = _heads_for_split(nsm, num_qg, split, -(-N // Bc), after_full_rounds)
     if H is None:
         pytest.skip(f"no head count splits the tail {split} ways on {nsm} SMs with Bc={Bc}")
-    q, k, v, mask = _adversarial(1, H, N, d, seed=split + d, all_masked_head=2)
+    q, k, v, mask = _adversarial(1, H, N, d, seed=split + d, all_masked_head=2 % H)
     extra = _fully_masked_rows(mask, False)
     rows = workloads.sample_rows(1, H, N, 1 / 16, seed=split, extra=extra)
     run_case(eta, 1, H, N, d, "bf16", False, Br=Br, Bc=Bc, mask=mask, rows=rows, qkv=(q, k, v))
