@@ -274,6 +274,11 @@ def measure_fwd(eta, w, steps, warmup, Br=0, Bc=0, cpu_target_s=3.0, naive=False
                            lse_dev=lse, extra_rows=extra)
     if naive:
         par["held_to_tol"] = False   # the materialising baseline is reported, not held to the tolerance
+    # device memory the calls themselves need: the peak over the timed region
+    # beyond what is allocated when it starts (inputs, outputs, workspace)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    held = torch.cuda.memory_allocated()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     clocks = ClockSampler(torch.cuda.current_device())
@@ -301,7 +306,7 @@ def measure_fwd(eta, w, steps, warmup, Br=0, Bc=0, cpu_target_s=3.0, naive=False
     achieved = w.flops / (mean_ms / 1e3) / 1e12
     alg_bytes = 4 * w.B * w.H * w.N * w.d * elem + 4 * w.B * w.H * w.N
     launches = 3 if naive else 1
-    peak_extra = torch.cuda.max_memory_allocated() - base_mem - resident - (flush.numel() if flush is not None else 0)
+    peak_extra = torch.cuda.max_memory_allocated() - held
     name = tag or (w.name if w.N == workloads.WORKLOADS.get(w.name, w).N else f"{w.name}@N{w.N}")
     line = {
         "metric": METRIC if not naive else "attn_naive_fwd (materialising baseline) TFLOP/s; max-abs error vs FP64 oracle",
@@ -319,7 +324,8 @@ def measure_fwd(eta, w, steps, warmup, Br=0, Bc=0, cpu_target_s=3.0, naive=False
                      "peak_source": f"{pk['source']} bf16 burst", "kernel_ms": mean_ms,
                      "kernel_ms_median": med_ms},
         "mem": {"resident_inputs_outputs_bytes": int(resident), "call_peak_extra_bytes": int(max(0, peak_extra)),
-                "workspace_bytes": int(ws.numel()) if ws is not None else 0},
+                "workspace_bytes": int(ws.numel()) if ws is not None else 0,
+                "per_call_bytes_beyond_inputs_outputs": int(ws.numel()) if ws is not None else 0},
         "gpu_launches": launches * steps,
         "clocks": clk,
         "cpu_baseline": cb,

@@ -53,7 +53,34 @@ EncodeTiledFn encode_tiled_fn() {
     return g_encode;
 }
 
+namespace {
+// Recently encoded tensor maps, keyed by (device, base, D, N, BH, box rows):
+// repeated calls on the same buffers (a training or benchmark loop) skip the
+// driver's encode.  A small table with round-robin replacement.
+struct MapEntry {
+    int dev, D, N, BH, box_rows;
+    const void *base;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 32;
+MapEntry g_maps[kMapCache];
+int g_maps_n = 0, g_maps_next = 0;
+std::mutex g_maps_mu;
+}  // namespace
+
 bool make_bf16_rows_map(CUtensorMap *m, const void *base, int D, int N, int BH, int box_rows) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    {
+        std::lock_guard<std::mutex> lk(g_maps_mu);
+        for (int i = 0; i < g_maps_n; ++i) {
+            const MapEntry &e = g_maps[i];
+            if (e.base == base && e.dev == dev && e.D == D && e.N == N && e.BH == BH && e.box_rows == box_rows) {
+                *m = e.map;
+                return true;
+            }
+        }
+    }
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
@@ -61,9 +88,22 @@ bool make_bf16_rows_map(CUtensorMap *m, const void *base, int D, int N, int BH, 
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
     const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lk(g_maps_mu);
+    MapEntry &e = g_maps[g_maps_next];
+    e.dev = dev;
+    e.D = D;
+    e.N = N;
+    e.BH = BH;
+    e.box_rows = box_rows;
+    e.base = base;
+    e.map = *m;
+    g_maps_next = (g_maps_next + 1) % kMapCache;
+    if (g_maps_n < kMapCache) ++g_maps_n;
+    return true;
 }
 
 int *device_error_word() {

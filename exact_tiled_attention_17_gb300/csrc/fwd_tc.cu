@@ -946,6 +946,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             if (nkvq > 0 && ok) ok = mbar_wait(bar(S::BAR_OFULL + q), uo & 1, abort_flag, p.err, 21);
             tc_fence_after();
             float a_own = 1.f;                 // weight of this CTA's O
+            float a_part[7];                   // weights of the other parts' O (0: nothing to add)
+#pragma unroll
+            for (int pp = 0; pp < 7; ++pp) a_part[pp] = 0.f;
             float l_fin = l, m_fin = m;
             bool parts_ok = false;             // the other parts' partials may be read
             bool write_out = true;
@@ -984,22 +987,28 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                     // A failed wait (the error word has it) reads no partial: the
                     // merge then has only this part's keys, and the O / LSE stores
                     // below are skipped because the abort flag is set.
-                    // (the parts' statistics are read again where needed rather
-                    // than held in registers)
+                    // Every part's (m, l) is read in one round trip over the
+                    // cluster (all loads issued before any is used).
                     parts_ok = mbar_wait_cluster(bar(S::BAR_PART), 0, abort_flag, p.err, 23);
-                    m_fin = m;
-                    for (int pp = 1; parts_ok && pp < nparts; ++pp)
-                        m_fin = fmaxf(m_fin, ld_cluster_f32(mapa_shared(stat_addr(0), pp)));
-                    if (m_fin == kNegInf) {
-                        a_own = 0.f;
-                        l_fin = 0.f;
-                    } else {
-                        a_own = (m == kNegInf) ? 0.f : ex2(m - m_fin);
-                        l_fin = a_own * l;
-                        for (int pp = 1; parts_ok && pp < nparts; ++pp) {
-                            const float mp = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
-                            if (mp != kNegInf) l_fin += ex2(mp - m_fin) * ld_cluster_f32(mapa_shared(stat_addr(1), pp));
+                    float mps[7], lps[7];
+#pragma unroll
+                    for (int pp = 1; pp < 8; ++pp) {
+                        mps[pp - 1] = kNegInf;
+                        lps[pp - 1] = 0.f;
+                        if (parts_ok && pp < nparts) {
+                            mps[pp - 1] = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
+                            lps[pp - 1] = ld_cluster_f32(mapa_shared(stat_addr(1), pp));
                         }
+                    }
+                    m_fin = m;
+#pragma unroll
+                    for (int pp = 0; pp < 7; ++pp) m_fin = fmaxf(m_fin, mps[pp]);
+                    a_own = (m == kNegInf || m_fin == kNegInf) ? 0.f : ex2(m - m_fin);
+                    l_fin = a_own * l;
+#pragma unroll
+                    for (int pp = 0; pp < 7; ++pp) {
+                        a_part[pp] = (mps[pp] == kNegInf || m_fin == kNegInf) ? 0.f : ex2(mps[pp] - m_fin);
+                        l_fin += a_part[pp] * lps[pp];
                     }
                 }
             }
@@ -1024,20 +1033,17 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                             // their shared memory through the cluster)
 #pragma unroll
                             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a_own);
-                            for (int pp = 1; parts_ok && pp < nparts; ++pp) {
-                                const float mp = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
-                                if (mp == kNegInf || m_fin == kNegInf) continue;
-                                const float ap = ex2(mp - m_fin);
-                                const uint32_t src = mapa_shared(part_row + 32 * c * 4, pp);
 #pragma unroll
-                                for (int k = 0; k < 8; ++k) {
-                                    float v0, v1, v2, v3;
-                                    ld_cluster_v4(src + 16 * k, v0, v1, v2, v3);
-                                    o[4 * k] = __float_as_uint(fmaf(ap, v0, __uint_as_float(o[4 * k])));
-                                    o[4 * k + 1] = __float_as_uint(fmaf(ap, v1, __uint_as_float(o[4 * k + 1])));
-                                    o[4 * k + 2] = __float_as_uint(fmaf(ap, v2, __uint_as_float(o[4 * k + 2])));
-                                    o[4 * k + 3] = __float_as_uint(fmaf(ap, v3, __uint_as_float(o[4 * k + 3])));
-                                }
+                            for (int pp = 1; pp < 8; ++pp) {
+                                const float ap = a_part[pp - 1];
+                                if (pp >= nparts || ap == 0.f) continue;
+                                const uint32_t src = mapa_shared(part_row + 32 * c * 4, pp);
+                                // the chunk's 8 loads are issued before the first is used
+                                float v[32];
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) ld_cluster_v4(src + 16 * k, v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(fmaf(ap, v[e], __uint_as_float(o[e])));
                             }
                         }
                     }
