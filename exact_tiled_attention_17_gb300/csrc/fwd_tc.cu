@@ -90,7 +90,10 @@ struct TcShape {
     // two warpgroups per tile exchange per-row values (half maxima, partial sums)
     static constexpr int XCH_BYTES = NH == 2 ? NQ * 2 * 128 * 8 : 0;
     // block-sparse: the listed key tiles (index | per-query-tile marks << 14) and per-tile counts
-    static constexpr int LIST_BYTES = BSPARSE ? kBsListCap * 2 + 16 : 0;
+    // block-sparse: three unit lists in rotation (a unit's list is built while
+    // the previous unit runs; no warp is ever two units behind another)
+    static constexpr int LIST_ONE = kBsListCap * 2 + 16;
+    static constexpr int LIST_BYTES = BSPARSE ? 3 * LIST_ONE : 0;
     static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES - MASK_BYTES - XCH_BYTES - LIST_BYTES) / SLOT_BYTES;
     static constexpr int NS = NS_RAW > 8 ? 8 : (NS_RAW < 2 ? 2 : NS_RAW);
     static constexpr int TMEM_USED = NQ * (NSB * BC + D);
@@ -134,7 +137,8 @@ struct TcShape {
     static constexpr int BAR_OFREE = BAR_QFREE + NQ;
     static constexpr int BAR_DONE = BAR_OFREE + NQ;
     static constexpr int BAR_PART = BAR_DONE + 1;       // split K/V: partials of the other parts are ready
-    static constexpr int NBARS = BAR_PART + 1;
+    static constexpr int BAR_LIST = BAR_PART + 1;       // block-sparse: unit list b is built (3)
+    static constexpr int NBARS = BAR_LIST + 3;
     // split K/V: a part's partial results, staged in the (then idle) Q tiles and K/V ring:
     // unnormalised O rows (float32, padded stride) and the per-row m, l
     static constexpr int PSTR = D + 4;
@@ -223,7 +227,10 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
     const int nkv_all = (N + BC - 1) / BC;
     const int cta = blockIdx.x;
     const int G = gridDim.x;
-    uint16_t *kv_list = reinterpret_cast<uint16_t *>(smem + S::OFF_LIST);
+    // block-sparse: the listed key tiles of unit u (index | per-query-tile marks
+    // << 14) and, after them, the per-query-tile list lengths
+    auto list_of = [&](int u) { return reinterpret_cast<uint16_t *>(smem + S::OFF_LIST + (u % 3) * S::LIST_ONE); };
+    uint16_t *kv_list = list_of(0);   // the current unit's list
 
     // ---- geometry of one work unit ----
     // Causal: heaviest query groups (largest rows) first.  Non-causal: all
@@ -234,7 +241,8 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
     int bh = 0, kv_lo = 0, nkv_max = 0;
     int r0[NQ], nkv[NQ];
     // (32-bit arithmetic only: nkv_all * 8 < 2^31, and nparts = 2^split_shift)
-    auto geometry = [&](int item, int part, int nparts) {
+    auto geometry = [&](int u, int item, int part, int nparts) {
+        if constexpr (BSPARSE) kv_list = list_of(u);
         const int dq = p.causal ? p.BH : p.num_qg;
         const int quo = item / dq, rem = item - quo * dq;
         const int qg = p.causal ? p.num_qg - 1 - quo : rem;
@@ -249,7 +257,8 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             if (r0[q] >= N) {
                 nkv[q] = 0;
             } else if constexpr (BSPARSE) {
-                nkv[q] = reinterpret_cast<const int *>(smem + S::OFF_LIST + kBsListCap * 2)[q];
+                // (clamped: after a failed wait the list may not have been built)
+                nkv[q] = min(max(reinterpret_cast<const int *>(kv_list + kBsListCap)[q], 0), kBsListCap);
             } else if (p.causal) {
                 const int last_row = min(r0[q] + BR - 1, N - 1);
                 nkv[q] = min(nkv_all, last_row / BC + 1);
@@ -284,6 +293,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         }
         mbar_init(bar(S::BAR_DONE), 1);
         mbar_init(bar(S::BAR_PART), static_cast<uint32_t>((p.split > 1 ? p.split - 1 : 1) * S::SOFTMAX_WARPS * 32));
+        for (int b = 0; b < 3; ++b) mbar_init(bar(S::BAR_LIST + b), 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -291,59 +301,68 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
         tmem_relinquish();
     }
-    if constexpr (BSPARSE) {
-        // One work unit per CTA (the launch makes one CTA per item).
-        int item0 = 0, part0 = 0, nparts0 = 1;
-        work_unit(p, cta, G, 0, item0, part0, nparts0);
-        const int qg = p.causal ? p.num_qg - 1 - item0 / p.BH : item0 % p.num_qg;
-        bh = p.causal ? item0 % p.BH : item0 / p.num_qg;
+    // Block-sparse: warp 1 builds unit u's list into buffer u % 3 (key tiles
+    // marked for at least one of the unit's query tiles, in order, with the
+    // per-tile marks in bits 14..15, and per query tile how many entries reach
+    // its last marked tile) and arrives on that buffer's barrier.  A query
+    // tile inside N with no marked tile still runs one fully masked tile,
+    // which writes O = 0 and LSE = -inf.
+    auto build_list = [&](int u) {
+        int item, part, nparts;
+        if (!work_unit(p, cta, G, u, item, part, nparts)) return;
+        const int dq = p.causal ? p.BH : p.num_qg;
+        const int quo = item / dq, rem = item - quo * dq;
+        const int qg = p.causal ? p.num_qg - 1 - quo : rem;
+        const int bhu = p.causal ? rem : quo;
+        int r0u[NQ];
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) r0[q] = (qg * NQ + q) * BR;
-        // Warp 1 lists the key tiles marked for at least one of the CTA's query
-        // tiles (in order, with the per-tile marks in bits 14..15) and, per
-        // query tile, how many list entries reach its last marked tile.  A
-        // query tile inside N with no marked tile still runs one fully masked
-        // tile, which writes O = 0 and LSE = -inf.
-        if (warp == 1) {
-            int *counts = reinterpret_cast<int *>(smem + S::OFF_LIST + kBsListCap * 2);
-            const int nkb = p.nkb;
-            const uint8_t *bm = p.block_mask + static_cast<size_t>(bh) * nkb * nkb;
-            int cnt = 0, last[NQ];
+        for (int q = 0; q < NQ; ++q) r0u[q] = (qg * NQ + q) * BR;
+        uint16_t *lst = list_of(u);
+        int *counts = reinterpret_cast<int *>(lst + kBsListCap);
+        const int nkb = p.nkb;
+        const uint8_t *bm = p.block_mask + static_cast<size_t>(bhu) * nkb * nkb;
+        int cnt = 0, last[NQ];
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) last[q] = 0;
-            for (int j0 = 0; j0 < nkb; j0 += 32) {
-                const int jt = j0 + lane;
-                uint32_t marks = 0;
+        for (int q = 0; q < NQ; ++q) last[q] = 0;
+        for (int j0 = 0; j0 < nkb; j0 += 32) {
+            const int jt = j0 + lane;
+            uint32_t marks = 0;
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    if (r0[q] < N && jt < nkb) {
-                        bool a = bm[static_cast<size_t>(r0[q] / 128) * nkb + jt] != 0;
-                        if (p.causal) a = a && (jt * BC <= min(r0[q] + BR - 1, N - 1));
-                        if (a) marks |= 1u << q;
-                    }
+            for (int q = 0; q < NQ; ++q) {
+                if (r0u[q] < N && jt < nkb) {
+                    bool a = bm[static_cast<size_t>(r0u[q] / 128) * nkb + jt] != 0;
+                    if (p.causal) a = a && (jt * BC <= min(r0u[q] + BR - 1, N - 1));
+                    if (a) marks |= 1u << q;
                 }
-                const uint32_t ball = __ballot_sync(0xffffffffu, marks != 0);
-                if (marks) kv_list[cnt + __popc(ball & ((1u << lane) - 1u))] = static_cast<uint16_t>(jt | (marks << 14));
+            }
+            const uint32_t ball = __ballot_sync(0xffffffffu, marks != 0);
+            if (marks) lst[cnt + __popc(ball & ((1u << lane) - 1u))] = static_cast<uint16_t>(jt | (marks << 14));
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    const uint32_t bq = __ballot_sync(0xffffffffu, (marks >> q) & 1u);
-                    if (bq) {
-                        const int L = 31 - __clz(bq);
-                        last[q] = cnt + __popc(ball & ((1u << L) - 1u)) + 1;
-                    }
+            for (int q = 0; q < NQ; ++q) {
+                const uint32_t bq = __ballot_sync(0xffffffffu, (marks >> q) & 1u);
+                if (bq) {
+                    const int L = 31 - __clz(bq);
+                    last[q] = cnt + __popc(ball & ((1u << L) - 1u)) + 1;
                 }
-                cnt += __popc(ball);
             }
-            bool empty_tile = false;
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) empty_tile = empty_tile || (r0[q] < N && last[q] == 0);
-            if (empty_tile && cnt == 0 && lane == 0) kv_list[0] = 0;
-            if (lane == 0) {
-#pragma unroll
-                for (int q = 0; q < NQ; ++q) counts[q] = (r0[q] < N && last[q] == 0) ? 1 : last[q];
-            }
+            cnt += __popc(ball);
         }
-    }
+        bool empty_tile = false;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) empty_tile = empty_tile || (r0u[q] < N && last[q] == 0);
+        if (empty_tile && cnt == 0 && lane == 0) lst[0] = 0;
+        if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) counts[q] = (r0u[q] < N && last[q] == 0) ? 1 : last[q];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(S::BAR_LIST + u % 3));
+    };
+    // Every role waits for unit u's list before reading it.
+    auto wait_list = [&](int u) -> bool {
+        if constexpr (BSPARSE) return mbar_wait(bar(S::BAR_LIST + u % 3), (u / 3) & 1, abort_flag, p.err, 26);
+        return true;
+    };
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -389,7 +408,13 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             for (int u = 0; ok; ++u) {
                 int item, part, nparts;
                 if (!work_unit(p, cta, G, u, item, part, nparts)) break;
-                geometry(item, part, nparts);
+                if constexpr (BSPARSE) {
+                    if (!wwait(bar(S::BAR_LIST + u % 3), (u / 3) & 1, 26)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                geometry(u, item, part, nparts);
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) {
                     if (nkv[q] == 0) continue;
@@ -500,7 +525,13 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             for (int u = 0; ok; ++u) {
                 int item, part, nparts;
                 if (!work_unit(p, cta, G, u, item, part, nparts)) break;
-                geometry(item, part, nparts);
+                if constexpr (BSPARSE) {
+                    if (!wwait(bar(S::BAR_LIST + u % 3), (u / 3) & 1, 26)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                geometry(u, item, part, nparts);
 #pragma unroll
                 for (int q = 0; q < NQ; ++q)
                     if (ok && nkv[q] > 0) ok = wwait(bar(S::BAR_QFULL + q), uo[q] & 1, 10);
@@ -655,7 +686,16 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         for (int u = 0;; ++u) {
             int item, part, nparts;
             if (!work_unit(p, cta, G, u, item, part, nparts)) break;
-            geometry(item, part, nparts);
+            if constexpr (BSPARSE) {
+                // warp 1 lists this unit's key tiles (the first unit) and the
+                // next unit's, while this one runs
+                if (warp == 1) {
+                    if (u == 0) build_list(0);
+                    build_list(u + 1);
+                }
+                if (!wait_list(u)) ok = false;
+            }
+            geometry(u, item, part, nparts);
             // This tile's row offset and K/V tile count as plain registers (a
             // run-time index into r0[] / nkv[] would place them in local memory).
             int r0q = r0[0], nkvq = nkv[0];
@@ -1184,9 +1224,8 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
     // Work: one CTA per SM, each running a list of work units (TcParams).
     // Non-causal items past the last full round are split along K/V into s
     // parts, s the largest power of two with s * (items mod SMs) <= SMs, run
-    // by clusters of s CTAs; causal work is uneven and stays unsplit.  The
-    // block-sparse variant runs one CTA per item.
-    long long grid = BSPARSE ? items : std::min<long long>(items, nsm);
+    // by clusters of s CTAs; causal and block-sparse work stays unsplit.
+    long long grid = std::min<long long>(items, nsm);
     long long n_full = items;
     int split = 1;
     if (S::CAN_SPLIT && !causal) {
@@ -1227,7 +1266,7 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
         p.n_full = p.items;
         p.split = 1;
         p.split_shift = 0;
-        grid = BSPARSE ? items : std::min<long long>(items, nsm);
+        grid = std::min<long long>(items, nsm);
     }
     if (split_out) *split_out = 1;
     kern<<<static_cast<unsigned>(grid), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, p);
