@@ -8,22 +8,28 @@
 // unnormalised accumulator that is multiplied by exp(m_old - m_new) when the
 // maximum grows, with one division at the end.
 //
-// GB300 mapping: one CTA per group of NQ consecutive BR-row query tiles of one
-// (batch, head); heaviest groups (largest row index, for causal) launch first.
+// GB300 mapping: at most one CTA per SM, each running a list of work units:
+// a group of NQ consecutive BR-row query tiles of one (batch, head), or one
+// part of such a group split along K/V (the last round; merged in a cluster).
+// Causal: heaviest groups (largest row index) first.
 //   warps 0 .. 4*NQ*NH-1  softmax warpgroups: NH per query tile (NH = 2 for
 //                  BC = 128: each owns half of the tile's key columns and half
 //                  of O's columns).  One thread per row (tensor-memory lane =
-//                  row).  Reads its S columns, applies scale and masks, keeps
-//                  the row state (m, l), rescales its O columns in tensor
-//                  memory when needed, writes its part of P as bf16 back over
-//                  its S columns, then the epilogue (normalise, bf16, TMA
-//                  store; LSE).
+//                  row).  Reads its S columns, applies the scale (and the
+//                  causal and length masks on edge tiles), keeps the row
+//                  state (m, l), rescales its O columns in tensor memory when
+//                  needed, writes its part of P as bf16 back over its S
+//                  columns, then the epilogue (normalise, bf16 stores; LSE).
 //   next warp      TMA producer: Q tiles once, then K_j / V_j tiles into a
-//                  ring of NS shared-memory slots (128-byte swizzle).
+//                  ring of NS shared-memory slots (128-byte swizzle); with a
+//                  key mask, also each K tile's mask / scale as a 16-wide bf16
+//                  operand (three exact parts per key).
 //   next warp      MMA issuer (one elected lane): S_q = Q_q K_j^T (both
-//                  operands in shared memory) and O_q += P_q V_j (P from tensor
-//                  memory, V MN-major in shared memory) on tcgen05, f32
-//                  accumulators in tensor memory.
+//                  operands in shared memory; with a key mask one more K step,
+//                  ones x mask operand, adds mask / scale to every row) and
+//                  O_q += P_q V_j (P from tensor memory, V MN-major in shared
+//                  memory) on tcgen05, f32 accumulators in tensor memory.
+//                  A masked tile thus reaches the softmax like any other.
 // The MMA issue order S_0(j+1) after P_0 V_j, S_1(j+1) after P_1 V_j lets the
 // tensor pipe work on one tile while the other tile's softmax runs; each half
 // of P is handed over as soon as its warpgroup has written it.  Where tensor
@@ -76,8 +82,14 @@ struct TcShape {
     static constexpr int Q_BYTES = BR * D * 2;      // one Q (or O staging) tile
     static constexpr int SLOT_BYTES = BC * D * 2;   // one K or V tile
     static constexpr int SMEM_BUDGET = 225 * 1024;  // leaves room for barriers and alignment
-    // key mask of the current tile in log2 units, double-buffered per query tile
-    static constexpr int MASK_BYTES = MASKED ? NQ * 2 * BC * 4 : 0;
+    // Key mask as one more K = 16 step of S = Q K^T: a constant A operand of
+    // ones (128 rows, k = 0..2 one, the rest zero) times a B operand holding
+    // each key's mask / scale as three bf16 parts (hi + mid + lo, k = 0..2).
+    // Both are K-major without swizzle: 32 bytes per row, 8-row groups of
+    // 256 bytes.  One B operand per ring slot (written with the K tile).
+    static constexpr int MOP_ROW = 32;
+    static constexpr int MOP_ONES = MASKED ? 128 * MOP_ROW : 0;
+    static constexpr int MOP_SLOT = MASKED ? BC * MOP_ROW : 0;
     // Two S buffers per query tile when tensor memory has room: S_q(j+2) is
     // computed while the softmax works on S_q(j+1) and P_q(j) waits for its
     // P V, instead of after P V.
@@ -94,8 +106,9 @@ struct TcShape {
     // the previous unit runs; no warp is ever two units behind another)
     static constexpr int LIST_ONE = kBsListCap * 2 + 16;
     static constexpr int LIST_BYTES = BSPARSE ? 3 * LIST_ONE : 0;
-    static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES - MASK_BYTES - XCH_BYTES - LIST_BYTES) / SLOT_BYTES;
+    static constexpr int NS_RAW = (SMEM_BUDGET - NQ * Q_BYTES - MOP_ONES - XCH_BYTES - LIST_BYTES) / (SLOT_BYTES + MOP_SLOT);
     static constexpr int NS = NS_RAW > 8 ? 8 : (NS_RAW < 2 ? 2 : NS_RAW);
+    static constexpr int MASK_BYTES = MOP_ONES + NS * MOP_SLOT;
     static constexpr int TMEM_USED = NQ * (NSB * BC + D);
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32
                                      : TMEM_USED <= 64 ? 64
@@ -104,6 +117,10 @@ struct TcShape {
     static constexpr int SOFTMAX_WARPS = 4 * NQ * NH;
     static constexpr int WARP_TMA = SOFTMAX_WARPS;
     static constexpr int WARP_MMA = SOFTMAX_WARPS + 1;
+    // key mask: one more warp writes each K tile's mask operand (off the
+    // TMA producer's path; with 18 or 10 other warps it costs no registers)
+    static constexpr int WARP_MASK = SOFTMAX_WARPS + 2;
+    static constexpr int EXTRA_WARPS = MASKED ? 3 : 2;
 
     // setmaxnreg could move registers from the producer/MMA warpgroup to the
     // softmax warpgroups; every shape here fits the launch share, and the
@@ -111,7 +128,7 @@ struct TcShape {
     static constexpr bool MOVE_REGS = false;
     // softmax warps + TMA + MMA (a whole warpgroup for those two when
     // registers are moved, since setmaxnreg acts per warpgroup)
-    static constexpr int THREADS = MOVE_REGS ? 32 * SOFTMAX_WARPS + 128 : 32 * (SOFTMAX_WARPS + 2);
+    static constexpr int THREADS = MOVE_REGS ? 32 * SOFTMAX_WARPS + 128 : 32 * (SOFTMAX_WARPS + EXTRA_WARPS);
     static constexpr int LAUNCH_REGS = NH == 2 ? 96 : 168;   // 65536 / THREADS, rounded down to 8
     static constexpr int REGS_SOFTMAX = NH == 2 ? 112 : 208;
     static constexpr int REGS_OTHER = NH == 2 ? 32 : 88;     // softmax + other shares == THREADS * LAUNCH_REGS
@@ -172,6 +189,7 @@ struct TcParams {
     int BH;             // B * H
     int num_qg;         // query groups (NQ * BR rows) per head
     int causal;
+    float scale;        // multiplies Q K^T
     float scale_log2;   // scale * log2(e)
     const float *key_mask;  // [BH][N] additive, or null
     const uint8_t *block_mask;  // block-sparse: [BH][nkb][nkb] bytes, non-zero = take part
@@ -288,7 +306,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             mbar_init(bar(S::BAR_OFREE + q), 128 * S::NH);
         }
         for (int s = 0; s < S::NS; ++s) {
-            mbar_init(bar(S::BAR_FULL + s), 1);
+            mbar_init(bar(S::BAR_FULL + s), MASKED ? 2 : 1);   // (+ the mask warp)
             mbar_init(bar(S::BAR_EMPTY + s), 1);
         }
         mbar_init(bar(S::BAR_DONE), 1);
@@ -363,6 +381,18 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         if constexpr (BSPARSE) return mbar_wait(bar(S::BAR_LIST + u % 3), (u / 3) & 1, abort_flag, p.err, 26);
         return true;
     };
+    if constexpr (MASKED) {
+        // The ones operand (16-byte unit i: k-chunk (i >> 3) & 1, whose chunk 0
+        // holds 1, 1, 1, 0 ... in bf16) and every slot's B operand zeroed (its
+        // k = 8..15 chunk stays zero; k = 0..7 is rewritten per K tile).
+        for (int i = threadIdx.x; i < S::MASK_BYTES / 16; i += S::THREADS) {
+            const bool one = i < S::MOP_ONES / 16 && ((i >> 3) & 1) == 0;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + S::OFF_MASK + 16 * i),
+                         "r"(one ? 0x3F803F80u : 0u), "r"(one ? 0x00003F80u : 0u), "r"(0u), "r"(0u)
+                         : "memory");
+        }
+        fence_proxy_async_smem();   // read by the tensor core
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -453,6 +483,80 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             for (int q = 0; q < NQ; ++q)
                 if (uo[q] > 0) wwait(bar(S::BAR_QFULL + q), (uo[q] - 1) & 1, 3);
             __syncwarp();
+        } else if (MASKED && warp == S::WARP_MASK) {
+            // --------------------------------------------------------------
+            // Key-mask operand: for each K tile, mask / scale of its keys as
+            // hi + mid + lo (bf16 each, round to nearest: 24 bits in all, so
+            // the float is exact), k = 0..2 of the slot's B operand.  A finite
+            // value past the bf16 range is clamped to it; -inf stays -inf with
+            // zero mid and lo.  Arrives on every slot's full barrier (V tiles
+            // too: the ring depth may be odd), the next K tile's values
+            // already fetched while the warp waits.
+            // --------------------------------------------------------------
+            constexpr int MPL = BC / 32;   // keys per lane
+            int t = 0;                     // K/V tiles so far, all units (as the producer counts)
+            bool ok = true;
+            for (int u = 0; ok; ++u) {
+                int item, part, nparts;
+                if (!work_unit(p, cta, G, u, item, part, nparts)) break;
+                if constexpr (BSPARSE) {
+                    if (!wwait(bar(S::BAR_LIST + u % 3), (u / 3) & 1, 26)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                geometry(u, item, part, nparts);
+                const float *mrow = p.key_mask + static_cast<size_t>(bh) * N;
+                float mv[MPL];
+                auto fetch = [&](int jj) {
+                    const int key0 = kv_tile(jj) * BC;
+#pragma unroll
+                    for (int i = 0; i < MPL; ++i) {
+                        const int key = key0 + 32 * i + lane;
+                        mv[i] = 0.f;
+                        if (key < N) asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(mv[i]) : "l"(mrow + key));
+                    }
+                };
+                if (nkv_max > 0) fetch(0);
+                for (int tt = 0; ok && tt < 2 * nkv_max; ++tt, ++t) {
+                    const int slot = t % S::NS, round = t / S::NS;
+                    if (round > 0 && !wwait(bar(S::BAR_EMPTY + slot), (round - 1) & 1, 5)) {
+                        ok = false;
+                        break;
+                    }
+                    if ((tt & 1) == 0) {
+                        const uint32_t mop = sbase + S::OFF_MASK + S::MOP_ONES + slot * S::MOP_SLOT;
+#pragma unroll
+                        for (int i = 0; i < MPL; ++i) {
+                            const int r = 32 * i + lane;
+                            float w = mv[i] / p.scale;
+                            constexpr float kBf16Max = 3.3895313892515355e38f;
+                            if (isinf(w) && !isinf(mv[i])) w = copysignf(kBf16Max, w);
+                            uint32_t w0, w1;
+                            if (isfinite(w)) {
+                                const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+                                const float r1 = w - __bfloat162float(hi);
+                                const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+                                const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+                                w0 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+                                     (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
+                                w1 = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
+                            } else {
+                                w0 = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(w)));
+                                w1 = 0u;
+                            }
+                            asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(mop + (r >> 3) * 256 + (r & 7) * 16),
+                                         "r"(w0), "r"(w1)
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();   // read by the tensor core
+                        __syncwarp();
+                        if ((tt >> 1) + 1 < nkv_max) fetch((tt >> 1) + 1);
+                    }
+                    if (leader) mbar_arrive(bar(S::BAR_FULL + slot));
+                }
+            }
+            __syncwarp();
         } else if (warp == S::WARP_MMA) {
             // --------------------------------------------------------------
             // MMA issuer (one elected lane)
@@ -464,6 +568,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
             const uint64_t kdesc0 = sdesc_sw128(sRing, 16, 1024);
             const uint64_t vdesc0 = sdesc_sw128(sRing, BC * 128, 1024);
+            // key mask: the ones operand and slot 0's mask operand
+            const uint64_t onesdesc = sdesc_kmajor_plain(sbase + S::OFF_MASK, 128, 256);
+            const uint64_t mopdesc0 = sdesc_kmajor_plain(sbase + S::OFF_MASK + S::MOP_ONES, 128, 256);
             // Running counts over all units: K/V tiles (t_base: the unit's K_0),
             // S tiles of each query tile, and units in which each query tile ran.
             int t_base = 0;
@@ -489,6 +596,10 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                                     b0 + static_cast<uint64_t>((cb * (BC * 128) + off) >> 4), idesc_s,
                                     kk > 0 ? 1u : 0u);
                     }
+                    if constexpr (MASKED)   // S += mask / scale
+                        mma_bf16_ss(tmem + S::s_col(q, b), onesdesc,
+                                    mopdesc0 + static_cast<uint64_t>((((t_base + 2 * j) % S::NS) * S::MOP_SLOT) >> 4),
+                                    idesc_s, 1u);
                     tc_commit(bar(S::BAR_SFULL + q * S::NSB + b));
                 }
                 if (j == nkvq - 1) commit(S::BAR_QFREE + q);
@@ -706,7 +817,6 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                     nkvq = nkv[i];
                 }
             const int row = r0q + row_in;
-            const float *mrow = MASKED ? p.key_mask + static_cast<size_t>(bh) * N : nullptr;
             float m = kNegInf;    // reference maximum, log2 units (the same in both warpgroups)
             float l = 0.f;        // sum of the bf16-rounded p over this warpgroup's columns
 
@@ -724,51 +834,20 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                 // block-sparse: a listed tile not marked for this query tile is masked whole
                 bool dead = false;
                 if constexpr (BSPARSE) dead = !((kv_list[j] >> (14 + q)) & 1);
-                // Tiles that need per-element masking: the N tail, the causal
-                // diagonal, or any tile when a key mask is given.
-                const bool edge = MASKED || dead || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0q);
+                // Tiles that need per-element masking: the N tail and the causal
+                // diagonal.  (A key mask is already part of S.)
+                const bool edge = dead || (key0 + BC > N) || (p.causal && key0 + BC - 1 > r0q);
 
                 const bool diag = p.causal && key0 + BC - 1 > r0q;   // tile crosses the causal diagonal
-                // Key mask of this warpgroup's columns, in log2 units with -inf
-                // past N; double-buffered so one barrier per tile suffices.
-                const float *msm = reinterpret_cast<const float *>(smem + S::OFF_MASK) + (q * 2 + (g & 1)) * BC;
-                if constexpr (MASKED) {
-                    // Staged by all 128 threads of the warpgroup (with M = 64 two
-                    // lanes share a row, so the row index would cover only half).
-                    float *mw = reinterpret_cast<float *>(smem + S::OFF_MASK) + (q * 2 + (g & 1)) * BC;
-#pragma unroll
-                    for (int t = h * CW + wq * 32 + lane; t < (h + 1) * CW; t += 128) {
-                        const int key = key0 + t;
-                        mw[t] = (key < N) ? __ldg(mrow + key) * kLog2e : kNegInf;
-                    }
-                    named_bar_sync(3 + q * S::NH + h, 128);
-                }
                 // One loaded 32-column chunk -> log2-domain scores
-                // x = s*scale*log2(e) (+ mask*log2(e)), -inf where not allowed.
+                // x = s*scale*log2(e), -inf where not allowed (past N, above
+                // the causal diagonal, a dead block-sparse tile).
                 auto mask_chunk = [&](int c, uint32_t *r) {
-                    if constexpr (MASKED) {
-                        // four staged mask values per broadcast load, two columns per f32x2 FMA
-                        const float4 *m4 = reinterpret_cast<const float4 *>(msm + 32 * c);
-                        const uint64_t sl2x2 = f2_pack(sl2, sl2);
-#pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 mv = m4[e4];
-                            float x0, x1, x2, x3;
-                            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1])), sl2x2,
-                                             f2_pack(mv.x, mv.y)), x0, x1);
-                            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3])), sl2x2,
-                                             f2_pack(mv.z, mv.w)), x2, x3);
-                            r[4 * e4] = __float_as_uint(x0);
-                            r[4 * e4 + 1] = __float_as_uint(x1);
-                            r[4 * e4 + 2] = __float_as_uint(x2);
-                            r[4 * e4 + 3] = __float_as_uint(x3);
-                        }
-                    }
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int key = key0 + 32 * c + e;
                         float x = __uint_as_float(r[e]);
-                        if constexpr (!MASKED) x = (key < N) ? x * sl2 : kNegInf;
+                        x = (key < N) ? x * sl2 : kNegInf;
                         if (diag) x = (key <= row) ? x : kNegInf;
                         if constexpr (BSPARSE) x = dead ? kNegInf : x;
                         r[e] = __float_as_uint(x);
@@ -860,6 +939,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
 #pragma unroll
                     for (int c = 0; c < NC; ++c) {
                         reg_fence32(sr[c]);
+                        if (!edge) reg_fence_f32(mxc[c]);
                         if (edge) {
                             mask_chunk(h * NC + c, sr[c]);
                             mx = chunk_max(sr[c], mx);
@@ -868,11 +948,15 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                         }
                     }
                     if (!edge) mx *= sl2;
+                    // (NH = 2: true when some row of the tile moves its reference;
+                    // the same in both warpgroups)
+                    bool any_move = false;
                     if constexpr (S::NH == 2) {
                         // The row maximum over both halves is needed only if some
                         // row's half maximum would move the reference: one vote,
                         // and the exchange only then.
-                        if (named_bar_red_or(7 + q, 256, active && mx > m + kRescaleThresh)) {
+                        any_move = named_bar_red_or(7 + q, 256, active && mx > m + kRescaleThresh);
+                        if (any_move) {
                             float mo, unused;
                             exchange(mx, 0.f, mo, unused);
                             mx = fmaxf(mx, mo);
@@ -909,6 +993,16 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                         o_settled();
                         rescale_o(a);
                     }
+                    if constexpr (S::NH == 2) {
+                        // Each half of P V accumulates into all of O's columns,
+                        // and each warpgroup rescales only its own: neither half
+                        // of P is handed over before both rescales are stored.
+                        if (j > 0 && any_move) {
+                            tmem_st_wait();
+                            tc_fence_before();
+                            pair_sync();
+                        }
+                    }
                     l = l * a + ls;
                     release_p();
                 } else {
@@ -929,6 +1023,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                             tmem_ld32_max(tS + h * CW + 32 * c, sr, mc);
                             tmem_ld_wait();
                             reg_fence32(sr);
+                            reg_fence_f32(mc);
                             mx = fmaxf(mx, mc);
                         }
                     }
@@ -1209,6 +1304,7 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
     p.BH = BH;
     p.num_qg = (N + NQ * BR - 1) / (NQ * BR);
     p.causal = causal;
+    p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.key_mask = key_mask;
     p.block_mask = block_mask;

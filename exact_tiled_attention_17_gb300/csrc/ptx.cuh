@@ -293,6 +293,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// Shared-memory matrix descriptor, no swizzle, K-major: 8-row x 16-byte core
+// matrices stored as 128 contiguous bytes; lbo = distance between core
+// matrices adjacent along K, sbo = between 8-row groups (layout field 0).
+__device__ __forceinline__ uint64_t sdesc_kmajor_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and f32 accumulate.
 // a_mn / b_mn select the MN-major ("transposed") operand layout.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
@@ -381,6 +393,9 @@ __device__ __forceinline__ void reg_fence32(uint32_t *r) {
                    "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
                    "+r"(r[31]));
 }
+// The same for one float (the maximum returned by tmem_ld32_max): without it
+// the compiler may read the register before tcgen05.wait::ld has filled it.
+__device__ __forceinline__ void reg_fence_f32(float &x) { asm volatile("" : "+f"(x)); }
 __device__ __forceinline__ void reg_fence16(uint32_t *r) {
     asm volatile(""
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),

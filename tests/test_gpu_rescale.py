@@ -6,18 +6,20 @@ denominator and an unnormalised accumulator, brought to a common maximum
 when a block with a larger one arrives), with two shortcuts that are exact up
 to rounding because O / l does not depend on the reference point:
 
-- key tiles of 64 or 128 columns: the reference maximum is the first tile's;
-  a later tile is exponentiated against it and redone against the row's new
-  maximum only if the p sum over one warpgroup's columns passes 2^16;
-- key tiles of 256 columns: the reference moves only when a tile's maximum
-  exceeds it by more than 8 (log2 units).
+- the reference maximum moves only to a tile maximum more than 8 (log2
+  units) above it, so a tile is exponentiated against a reference that may
+  lie below its maximum, every p stays below 2^8, and O is rescaled only when
+  the reference moves;
+- the row's denominator is the sum of the bf16-rounded p that P V applies.
 
-These tests put row scores just below and just above both limits, on every
+These tests put row scores just below and just above the limit, on every
 (d, Br, Bc) variant, causal and not, through exact embeddings (q = e0 plus a
 small second component, k_j = s_j e0 plus a small second component, scale =
 ln 2 so that a score is its own log2-domain value).  They also run the
 adversarial workload's generator (Q and K x30, -inf key padding, fully
-masked rows) through every variant and through the K/V-split cluster tail.
+masked rows) through every variant and through the K/V-split cluster tail,
+and run CTAs through several work units repeatedly: the results must be
+bitwise the same every time.
 Bar: the forward's bf16 tolerance against the FP64 oracle (O max-abs 2e-2;
 LSE 1e-3 + 2^-8 + 2e-6 |LSE|; fully masked rows O = 0, LSE = -inf).
 """
@@ -167,3 +169,40 @@ def test_adversarial_logits_split_tail(eta, d, Bc, split, after_full_rounds):
     # the same heads unmasked, N(0, 1) inputs
     run_case(eta, 1, H, N, d, "bf16", False, Br=Br, Bc=Bc, rows=rows, seed=split)
     assert f"_kvsplit{split}" in eta.attn_last_variant()
+
+
+@pytest.mark.parametrize("mask_kind", ["none", "zero", "padding"])
+@pytest.mark.parametrize("d,Bc", [(64, 128), (128, 128), (64, 64)])
+def test_repeated_runs_bitwise_identical(eta, d, Bc, mask_kind):
+    """x30 logits (the reference moves often) with every CTA running at least
+    two work units, repeated: every run bitwise equal to the first, and the
+    first within tolerance of the oracle.  (A row maximum read from a
+    tensor-memory load before the load has completed made this vary between
+    runs.)"""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    N, Br = 1000, 128
+    nq = 2 if 2 * (Bc + d) <= 512 else 1
+    num_qg = -(-N // (nq * Br))
+    H = -(-2 * nsm // num_qg)
+    q, k, v, mask = _adversarial(1, H, N, d, seed=d + Bc, all_masked_head=2)
+    if mask_kind == "zero":
+        mask = torch.zeros_like(mask)
+    elif mask_kind == "none":
+        mask = None
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = mask.to(dev) if mask is not None else None
+    scale = 1.0 / math.sqrt(d)
+    first = None
+    for rep in range(6):
+        o, lse = eta.attn_fwd(qd, kd, vd, False, scale, Br, Bc, md)
+        torch.cuda.synchronize()
+        assert eta.attn_status() == eta.ATTN_OK
+        if first is None:
+            first = (o.clone(), lse.clone())
+        else:
+            assert torch.equal(o, first[0]), f"run {rep}: O differs from the first run"
+            assert torch.equal(lse, first[1]), f"run {rep}: LSE differs from the first run"
+    extra = _fully_masked_rows(mask, False) if mask is not None else []
+    rows = workloads.sample_rows(1, H, N, 1 / 32, seed=d, extra=extra)
+    run_case(eta, 1, H, N, d, "bf16", False, Br=Br, Bc=Bc, mask=mask, rows=rows, qkv=(q, k, v))
