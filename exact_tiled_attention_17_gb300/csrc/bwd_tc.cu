@@ -39,7 +39,10 @@
 // Tensor memory (512 columns for d = 128):
 //   S^T | dP^T (64 each) | P^T | dS^T (bf16, 32 each) | dV | dK (d each) | dQ^T (64).
 #include <cuda_bf16.h>
+
+#include <atomic>
 #include <cstdio>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -564,13 +567,20 @@ int launch_bwd_d(const void *Q, const void *K, const void *V, const void *O, con
                  void *workspace, cudaStream_t stream) {
     using S = BwdShape<D>;
     auto kern = attn_bwd_tc_kernel<D>;
-    static int attr_device = -1;
+    // The shared-memory opt-in, once per device (calls may come from several
+    // host threads).
+    constexpr int kMaxDevBw = 64;
+    static std::atomic<int> ready[kMaxDevBw];
+    static std::mutex mu;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
-    if (attr_device != dev) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES) != cudaSuccess)
-            return kErrCuda;
-        attr_device = dev;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevBw) return kErrCuda;
+    if (ready[dev].load(std::memory_order_acquire) == 0) {
+        std::lock_guard<std::mutex> lk(mu);
+        if (ready[dev].load(std::memory_order_relaxed) == 0) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES) != cudaSuccess)
+                return kErrCuda;
+            ready[dev].store(1, std::memory_order_release);
+        }
     }
     const int npad = npad_of(N);
     char *ws = static_cast<char *>(workspace);
