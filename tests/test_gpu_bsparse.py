@@ -94,3 +94,18 @@ def test_bsparse_rejects(eta):
         eta.attn_fwd_block_sparse(qb, qb, qb, bm)              # d = 96
     with pytest.raises(ValueError):
         eta.attn_fwd_block_sparse(q.bfloat16(), q.bfloat16(), q.bfloat16(), bm[:, :, :1])   # wrong mask size
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bsparse_finite_key_mask(eta, d):
+    """Finite key-mask values (ordinary, tiny, large negative, -inf) on top of
+    a random block mask: the mask enters S inside the MMA as in the dense path."""
+    B, H, N = 1, 3, 1000
+    g = torch.Generator().manual_seed(d)
+    key_mask = torch.empty(B, H, N).uniform_(-6.0, 3.0, generator=g)
+    sel = torch.rand(B, H, N, generator=g)
+    key_mask = torch.where(sel < 0.05, torch.full_like(key_mask, float("-inf")), key_mask)
+    key_mask = torch.where((sel >= 0.05) & (sel < 0.10), key_mask - 200.0, key_mask)
+    bm = workloads.make_block_mask(B, H, N, 0.5, seed=d + 1)
+    _check(eta, B, H, N, d, False, bm, seed=d + 2, key_mask=key_mask)
+    _check(eta, B, H, N, d, True, bm, seed=d + 3, key_mask=key_mask)

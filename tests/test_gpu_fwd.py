@@ -204,3 +204,58 @@ def test_invalid_arguments_on_device(eta):
     with pytest.raises(eta.AttnError) as ei:
         eta.attn_fwd(q, q, q)
     assert ei.value.status == eta.ATTN_ERR_UNSUPPORTED
+
+
+# ---------------- finite key-mask values (the mask enters S inside the MMA) ----------------
+
+def _finite_mask(B, H, N, seed):
+    """Additive key mask with finite values of every kind, not only 0 / -inf:
+    ordinary values in [-6, 3), tiny ones (~1e-30), keys pushed down by ~200
+    (their weights underflow), values not representable in bf16, and 5% -inf."""
+    g = torch.Generator().manual_seed(seed)
+    m = torch.empty(B, H, N).uniform_(-6.0, 3.0, generator=g)
+    sel = torch.rand(B, H, N, generator=g)
+    m = torch.where(sel < 0.05, torch.full_like(m, float("-inf")), m)
+    m = torch.where((sel >= 0.05) & (sel < 0.10), m * 1e-30, m)
+    m = torch.where((sel >= 0.10) & (sel < 0.15), m - 200.0, m)
+    return m
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Br", [64, 128])
+@pytest.mark.parametrize("Bc", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_finite_key_mask(eta, d, Br, Bc, causal):
+    """Every (d, Br, Bc) variant with finite mask values: the tensor-core path
+    adds mask / scale to q.k as three bf16 parts in one more MMA step, which
+    must carry each float32 value (tiny, ordinary, large) to the scores."""
+    B, H, N = 1, 3, 700
+    mask = _finite_mask(B, H, N, seed=d + Bc + Br)
+    run_case(eta, B, H, N, d, "bf16", causal, Br=Br, Bc=Bc, mask=mask, seed=d + Br)
+    assert "_mask" in eta.attn_last_variant()
+
+
+@pytest.mark.parametrize("scale", [0.0625, 0.25, 2.0])
+def test_bf16_finite_key_mask_scales(eta, scale):
+    """The MMA adds mask / scale; the softmax multiplies by scale again: the
+    result must be scale * q.k + mask for small and large scales."""
+    B, H, N, d = 1, 2, 513, 128
+    mask = _finite_mask(B, H, N, seed=11)
+    run_case(eta, B, H, N, d, "bf16", False, mask=mask, seed=12, scale=scale)
+    run_case(eta, B, H, N, d, "bf16", True, mask=mask, seed=13, scale=scale)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Bc", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_zero_mask_bitwise_equals_no_mask(eta, d, Bc, causal):
+    """A zero key mask adds exactly 0 to every score (the extra MMA step's
+    products are all 0): O and LSE are bitwise those of the unmasked call."""
+    q, k, v = (t.cuda() for t in workloads.make_qkv(1, 3, 1000, d, "bf16", d + Bc))
+    zero = torch.zeros(1, 3, 1000, device="cuda")
+    o0, l0 = eta.attn_fwd(q, k, v, causal, 1 / math.sqrt(d), 128, Bc)
+    o1, l1 = eta.attn_fwd(q, k, v, causal, 1 / math.sqrt(d), 128, Bc, zero)
+    torch.cuda.synchronize()
+    assert "_mask" in eta.attn_last_variant()
+    assert torch.equal(o0, o1)
+    assert torch.equal(l0, l1)
