@@ -259,3 +259,19 @@ def test_bf16_zero_mask_bitwise_equals_no_mask(eta, d, Bc, causal):
     assert "_mask" in eta.attn_last_variant()
     assert torch.equal(o0, o1)
     assert torch.equal(l0, l1)
+
+
+def test_host_buffers_with_key_mask_match_device_call(eta):
+    """The host-memory entry copies Q, K, V and the key mask into its
+    workspace and runs the same kernel: O and LSE are bitwise those of the
+    device-buffer call, and within tolerance of the oracle."""
+    B, H, N, d = 1, 3, 450, 128
+    q, k, v = workloads.make_qkv(B, H, N, d, "bf16", 21)
+    mask = _finite_mask(B, H, N, seed=21)
+    oh, lh = eta.attn_fwd(q.pin_memory(), k.pin_memory(), v.pin_memory(), True, 0.1, key_mask=mask.pin_memory())
+    assert oh.device.type == "cpu" and lh.device.type == "cpu"
+    od, ld = eta.attn_fwd(q.cuda(), k.cuda(), v.cuda(), True, 0.1, key_mask=mask.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(oh, od.cpu())
+    assert torch.equal(lh, ld.cpu())
+    run_case(eta, B, H, N, d, "bf16", True, mask=mask, scale=0.1, qkv=(q, k, v))
