@@ -109,3 +109,14 @@ def test_bsparse_finite_key_mask(eta, d):
     bm = workloads.make_block_mask(B, H, N, 0.5, seed=d + 1)
     _check(eta, B, H, N, d, False, bm, seed=d + 2, key_mask=key_mask)
     _check(eta, B, H, N, d, True, bm, seed=d + 3, key_mask=key_mask)
+
+
+def test_bsparse_longest_list(eta):
+    """N = 131072: 1024 key blocks, the length a unit's key-tile list can
+    hold; a sliding window plus block 0, and one query block marking every
+    key block (its unit lists all 1024 tiles)."""
+    B, H, N, d = 1, 1, 131072, 64
+    bm = workloads.make_block_mask(B, H, N, pattern="local", window=1)
+    bm[0, 0, 500, :] = 1
+    rows = workloads.sample_rows(B, H, N, 32 / N, seed=3, extra=[500 * 128, 500 * 128 + 127, N - 1])
+    _check(eta, B, H, N, d, False, bm, seed=5, rows=rows)

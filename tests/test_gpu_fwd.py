@@ -275,3 +275,21 @@ def test_host_buffers_with_key_mask_match_device_call(eta):
     assert torch.equal(oh, od.cpu())
     assert torch.equal(lh, ld.cpu())
     run_case(eta, B, H, N, d, "bf16", True, mask=mask, scale=0.1, qkv=(q, k, v))
+
+
+# ---------------- long sequences (32-bit index arithmetic, many key tiles) ----------------
+
+def test_bf16_long_sequence_noncausal(eta):
+    """1 x 2 x 131072 x 64 non-causal (1024 key tiles per row, split tail);
+    oracle on a seeded row sample with each head's first and last rows."""
+    B, H, N, d = 1, 2, 131072, 64
+    rows = workloads.sample_rows(B, H, N, 48 / (B * H * N), seed=1)
+    run_case(eta, B, H, N, d, "bf16", False, rows=rows, seed=31)
+
+
+def test_bf16_long_sequence_causal_masked(eta):
+    """1 x 1 x 65536 x 128 causal with finite key-mask values and -inf keys."""
+    B, H, N, d = 1, 1, 65536, 128
+    mask = _finite_mask(B, H, N, seed=32)
+    rows = workloads.sample_rows(B, H, N, 48 / (B * H * N), seed=2, extra=[N - 2, N // 2])
+    run_case(eta, B, H, N, d, "bf16", True, mask=mask, rows=rows, seed=32)
