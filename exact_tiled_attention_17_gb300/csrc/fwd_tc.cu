@@ -31,8 +31,9 @@
 //                  memory) on tcgen05, f32 accumulators in tensor memory.
 //                  A masked tile thus reaches the softmax like any other.
 // The MMA issue order S_0(j+1) after P_0 V_j, S_1(j+1) after P_1 V_j lets the
-// tensor pipe work on one tile while the other tile's softmax runs; each half
-// of P is handed over as soon as its warpgroup has written it.  Where tensor
+// tensor pipe work on one tile while the other tile's softmax runs.  P_q is
+// handed over on one barrier that both warpgroups of the tile arrive on, so
+// the MMA warp wakes once per tile (waking once per warpgroup cost ~3%).  Where tensor
 // memory has room (BC = 64) each query tile has two S buffers and S_q(j+2) is
 // issued right after P_q V_j, so the softmax never waits for its own P V.
 //
@@ -96,8 +97,7 @@ struct TcShape {
     static constexpr bool DBS = 2 * NQ * BC + NQ * D <= 512;
     static constexpr int NSB = DBS ? 2 : 1;
     // BC = 128: two softmax warpgroups share each query tile, one per half of
-    // its columns (and of O's columns); each hands its half of P to the MMA as
-    // soon as it is written.
+    // its columns (and of O's columns).
     static constexpr int NH = BC == 128 ? 2 : 1;
     // two warpgroups per tile exchange per-row values (half maxima, partial sums)
     static constexpr int XCH_BYTES = NH == 2 ? NQ * 2 * 128 * 8 : 0;
@@ -146,7 +146,7 @@ struct TcShape {
     static constexpr int BAR_EMPTY = BAR_FULL + NS;
     static constexpr int BAR_SFULL = BAR_EMPTY + NS;
     static constexpr int BAR_PFULL = BAR_SFULL + NQ * NSB;
-    static constexpr int BAR_OFULL = BAR_PFULL + NQ * NSB * NH;
+    static constexpr int BAR_OFULL = BAR_PFULL + NQ * NSB;
     static constexpr int BAR_PVDONE = BAR_OFULL + NQ;   // two S buffers: each P_q V has completed
     // A CTA runs several work units: Q_q may be reloaded once the unit's last
     // S_q product has completed, and O_q rewritten once the epilogue has read it.
@@ -298,7 +298,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
             mbar_init(bar(S::BAR_QFULL + q), 1);
             for (int b = 0; b < S::NSB; ++b) {
                 mbar_init(bar(S::BAR_SFULL + q * S::NSB + b), 1);
-                for (int h = 0; h < S::NH; ++h) mbar_init(bar(S::BAR_PFULL + (q * S::NSB + b) * S::NH + h), 128);
+                // every softmax thread of the tile (both warpgroups): the MMA
+                // warp wakes once per tile, not once per warpgroup
+                mbar_init(bar(S::BAR_PFULL + q * S::NSB + b), 128 * S::NH);
             }
             mbar_init(bar(S::BAR_OFULL + q), 1);
             mbar_init(bar(S::BAR_PVDONE + q), 1);
@@ -621,12 +623,12 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                 }
             };
             // Before the unit's first P_q V (which overwrites O_q): the previous
-            // unit's epilogue has read O_q.  Then both halves of P_q(j).
-            auto wait_p = [&](int q, int j, int h) -> bool {
-                if (j == 0 && h == 0 && uo[q] > 0 && !wwait(bar(S::BAR_OFREE + q), (uo[q] - 1) & 1, 16))
+            // unit's epilogue has read O_q.  Then all of P_q(j).
+            auto wait_p = [&](int q, int j) -> bool {
+                if (j == 0 && uo[q] > 0 && !wwait(bar(S::BAR_OFREE + q), (uo[q] - 1) & 1, 16))
                     return false;
                 const int g = sq[q] + j;
-                if (!wwait(bar(S::BAR_PFULL + (q * S::NSB + (g & (S::NSB - 1))) * S::NH + h), (g / S::NSB) & 1, 13))
+                if (!wwait(bar(S::BAR_PFULL + q * S::NSB + (g & (S::NSB - 1))), (g / S::NSB) & 1, 13))
                     return false;
                 tc_fence_after();
                 return true;
@@ -683,11 +685,11 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
 #pragma unroll
                         for (int q = 0; q < NQ; ++q) {
                             if (!ok || j >= nkv[q]) continue;
+                            if (wait_p(q, j)) {
 #pragma unroll
-                            for (int h = 0; h < S::NH; ++h) {
-                                if (!ok) continue;
-                                if (wait_p(q, j, h)) issue_pv(q, j, h);
-                                else ok = false;
+                                for (int h = 0; h < S::NH; ++h) issue_pv(q, j, h);
+                            } else {
+                                ok = false;
                             }
                             if (!ok) continue;
                             commit(S::BAR_PVDONE + q);
@@ -725,11 +727,11 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
 #pragma unroll
                         for (int q = 0; q < NQ; ++q) {
                             if (!ok || j >= nkv[q]) continue;
+                            if (wait_p(q, j)) {
 #pragma unroll
-                            for (int h = 0; h < S::NH; ++h) {
-                                if (!ok) continue;
-                                if (wait_p(q, j, h)) issue_pv(q, j, h);
-                                else ok = false;
+                                for (int h = 0; h < S::NH; ++h) issue_pv(q, j, h);
+                            } else {
+                                ok = false;
                             }
                             if (!ok) continue;
                             if (j == nkv[q] - 1) commit(S::BAR_OFULL + q);
@@ -915,11 +917,14 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                         tc_fence_after();
                     }
                 };
-                // This warpgroup's part of P_q is in tensor memory: its P V may be issued.
+                // This warpgroup's part of P_q is in tensor memory (and its part
+                // of O rescaled): once both warpgroups have arrived, P_q V may
+                // be issued.  (Each half of P V accumulates into all of O's
+                // columns, so it must not start before both rescales.)
                 auto release_p = [&]() {
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(bar(S::BAR_PFULL + (q * S::NSB + sb) * S::NH + h));
+                    mbar_arrive(bar(S::BAR_PFULL + q * S::NSB + sb));
                 };
                 constexpr int NC = CW / 32;   // 32-column chunks of this warpgroup
                 if constexpr (NC <= 2) {
@@ -948,15 +953,11 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                         }
                     }
                     if (!edge) mx *= sl2;
-                    // (NH = 2: true when some row of the tile moves its reference;
-                    // the same in both warpgroups)
-                    bool any_move = false;
                     if constexpr (S::NH == 2) {
                         // The row maximum over both halves is needed only if some
                         // row's half maximum would move the reference: one vote,
                         // and the exchange only then.
-                        any_move = named_bar_red_or(7 + q, 256, active && mx > m + kRescaleThresh);
-                        if (any_move) {
+                        if (named_bar_red_or(7 + q, 256, active && mx > m + kRescaleThresh)) {
                             float mo, unused;
                             exchange(mx, 0.f, mo, unused);
                             mx = fmaxf(mx, mo);
@@ -992,16 +993,6 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                     if (j > 0 && __any_sync(0xffffffffu, moved)) {
                         o_settled();
                         rescale_o(a);
-                    }
-                    if constexpr (S::NH == 2) {
-                        // Each half of P V accumulates into all of O's columns,
-                        // and each warpgroup rescales only its own: neither half
-                        // of P is handed over before both rescales are stored.
-                        if (j > 0 && any_move) {
-                            tmem_st_wait();
-                            tc_fence_before();
-                            pair_sync();
-                        }
                     }
                     l = l * a + ls;
                     release_p();
