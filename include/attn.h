@@ -37,9 +37,10 @@
  *                sentinel anywhere in the library: the aicompass.dev note on
  *                FlashInfer kernels shows why a hard-coded -50,000 is wrong.
  *                On the bf16 tensor-core path the mask enters the score
- *                product: mask / scale, split into three bf16 parts that
- *                carry the float32 value exactly, is added to q.k before the
- *                scale is applied (equal to scale * q.k + mask up to float32
+ *                product: mask / scale (formed as mask times the float32
+ *                reciprocal of scale), split into three bf16 parts that carry
+ *                that float32 value exactly, is added to q.k before the scale
+ *                is applied (equal to scale * q.k + mask up to float32
  *                rounding); a finite mask / scale beyond the bf16 range
  *                (about 3.39e38) is clamped to it.
  *   A row whose every score is -inf (fully masked) outputs O = 0 and
