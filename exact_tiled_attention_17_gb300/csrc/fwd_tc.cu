@@ -20,22 +20,25 @@
 //                  state (m, l), rescales its O columns in tensor memory when
 //                  needed, writes its part of P as bf16 back over its S
 //                  columns, then the epilogue (normalise, bf16 stores; LSE).
-//   next warp      TMA producer: Q tiles once, then K_j / V_j tiles into a
-//                  ring of NS shared-memory slots (128-byte swizzle); with a
-//                  key mask, also each K tile's mask / scale as a 16-wide bf16
-//                  operand (three exact parts per key).
+//   next warp      TMA producer: each unit's Q tiles, then K_j / V_j tiles
+//                  into a ring of NS shared-memory slots (128-byte swizzle).
 //   next warp      MMA issuer (one elected lane): S_q = Q_q K_j^T (both
 //                  operands in shared memory; with a key mask one more K step,
 //                  ones x mask operand, adds mask / scale to every row) and
 //                  O_q += P_q V_j (P from tensor memory, V MN-major in shared
 //                  memory) on tcgen05, f32 accumulators in tensor memory.
-//                  A masked tile thus reaches the softmax like any other.
+//   next warp      (with a key mask) writes each K tile's mask / scale into
+//                  the ring slot as a 16-wide bf16 operand, three exact parts
+//                  per key, and arrives on the slot's full barrier too.  A
+//                  masked tile thus reaches the softmax like any other.
 // The MMA issue order S_0(j+1) after P_0 V_j, S_1(j+1) after P_1 V_j lets the
 // tensor pipe work on one tile while the other tile's softmax runs.  P_q is
 // handed over on one barrier that both warpgroups of the tile arrive on, so
-// the MMA warp wakes once per tile (waking once per warpgroup cost ~3%).  Where tensor
-// memory has room (BC = 64) each query tile has two S buffers and S_q(j+2) is
-// issued right after P_q V_j, so the softmax never waits for its own P V.
+// the MMA warp wakes once per tile (waking once per warpgroup cost ~3%), and
+// P_q V starts only after both warpgroups have rescaled their O columns.
+// Where tensor memory has room (BC = 64) each query tile has two S buffers
+// and S_q(j+2) is issued right after P_q V_j, so the softmax never waits for
+// its own P V.
 //
 // BR = 64 uses M = 64 MMAs, whose accumulator rows r sit in tensor-memory lane
 // 32*(r/16) + r%16: lanes 0..15 of each warp carry rows, lanes 16..31 idle.
@@ -53,9 +56,10 @@
 //
 // Block-sparse variant (BSPARSE): a byte mask over 128 x 128 (query block, key
 // block) pairs says which blocks take part; every other score is -inf.  The
-// CTA runs only the key tiles marked for at least one of its query tiles (a
-// list built at the start); a listed tile that is not marked for a query tile
-// is masked whole for it.
+// unit runs only the key tiles marked for at least one of its query tiles (a
+// list that one warp builds while the previous unit runs, in one of three
+// rotating buffers); a listed tile that is not marked for a query tile is
+// masked whole for it.
 #include <cuda_bf16.h>
 
 #include <algorithm>
