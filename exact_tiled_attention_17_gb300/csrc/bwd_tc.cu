@@ -512,17 +512,26 @@ __global__ void attn_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O, const 
         return;
     }
     const size_t row = static_cast<size_t>(bh) * N + i;
-    constexpr int PER = D / 32;   // elements per lane (2 or 4)
-    const __nv_bfloat16 *o = O + row * D + lane * PER;
-    const __nv_bfloat16 *g = dO + row * D + lane * PER;
+    constexpr int PER = D / 32;   // elements per lane (2 or 4), one vector load each
     float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
+    if constexpr (PER == 4) {
+        const uint2 ov = *reinterpret_cast<const uint2 *>(O + row * D + lane * PER);
+        const uint2 gv = *reinterpret_cast<const uint2 *>(dO + row * D + lane * PER);
+        acc = fmaf(bf16lo_to_f32(ov.x), bf16lo_to_f32(gv.x), acc);
+        acc = fmaf(bf16hi_to_f32(ov.x), bf16hi_to_f32(gv.x), acc);
+        acc = fmaf(bf16lo_to_f32(ov.y), bf16lo_to_f32(gv.y), acc);
+        acc = fmaf(bf16hi_to_f32(ov.y), bf16hi_to_f32(gv.y), acc);
+    } else {
+        const uint32_t ov = *reinterpret_cast<const uint32_t *>(O + row * D + lane * PER);
+        const uint32_t gv = *reinterpret_cast<const uint32_t *>(dO + row * D + lane * PER);
+        acc = fmaf(bf16lo_to_f32(ov), bf16lo_to_f32(gv), acc);
+        acc = fmaf(bf16hi_to_f32(ov), bf16hi_to_f32(gv), acc);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     float *z = dq_acc + row * D + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) z[e] = 0.f;
+    if constexpr (PER == 4) *reinterpret_cast<float4 *>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
+    else *reinterpret_cast<float2 *>(z) = make_float2(0.f, 0.f);
     if (lane == 0) {
         const float l = LSE[row];
         lse2[srow] = (l == kNegInfBw) ? kPosInfBw : l * kLog2eBw;
