@@ -293,3 +293,14 @@ def test_bf16_long_sequence_causal_masked(eta):
     mask = _finite_mask(B, H, N, seed=32)
     rows = workloads.sample_rows(B, H, N, 48 / (B * H * N), seed=2, extra=[N - 2, N // 2])
     run_case(eta, B, H, N, d, "bf16", True, mask=mask, rows=rows, seed=32)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 31, 127, 129, 255, 257])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_finite_key_mask_ragged(eta, N, d):
+    """Ragged lengths with finite mask values: the mask operand of the last
+    K tile holds the mask for keys < N only, and zeros past N."""
+    B, H = 1, 2
+    mask = _finite_mask(B, H, N, seed=N + d)
+    run_case(eta, B, H, N, d, "bf16", N % 2 == 1, mask=mask, seed=N + d)
+    run_case(eta, B, H, N, d, "bf16", N % 2 == 0, mask=mask, seed=N + d + 1)

@@ -206,3 +206,24 @@ def test_repeated_runs_bitwise_identical(eta, d, Bc, mask_kind):
     extra = _fully_masked_rows(mask, False) if mask is not None else []
     rows = workloads.sample_rows(1, H, N, 1 / 32, seed=d, extra=extra)
     run_case(eta, 1, H, N, d, "bf16", False, Br=Br, Bc=Bc, mask=mask, rows=rows, qkv=(q, k, v))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_masked_split_tail_two_batches(eta, d):
+    """B = 2 with finite key-mask values and -inf keys, heads chosen so that
+    the non-causal tail splits along K/V: each (batch, head) reads its own
+    mask row in every part."""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    N, Br, Bc = 1000, 128, 128
+    num_qg = -(-N // (2 * Br))
+    H = _heads_for_split(nsm, num_qg, 2, -(-N // Bc), True)
+    if H is None or H % 2:
+        pytest.skip("no even head count splits the tail 2 ways on this GPU")
+    B, Hh = 2, H // 2
+    g = torch.Generator().manual_seed(d)
+    mask = torch.empty(B, Hh, N).uniform_(-6.0, 3.0, generator=g)
+    sel = torch.rand(B, Hh, N, generator=g)
+    mask = torch.where(sel < 0.05, torch.full_like(mask, float("-inf")), mask)
+    rows = workloads.sample_rows(B, Hh, N, 1 / 16, seed=d)
+    run_case(eta, B, Hh, N, d, "bf16", False, Br=Br, Bc=Bc, mask=mask, rows=rows, seed=d)
+    assert "_kvsplit2" in eta.attn_last_variant()
