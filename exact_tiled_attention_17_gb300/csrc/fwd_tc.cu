@@ -161,9 +161,10 @@ struct TcShape {
     static constexpr int BAR_LIST = BAR_PART + 1;       // block-sparse: unit list b is built (3)
     static constexpr int NBARS = BAR_LIST + 3;
     // split K/V: a part's partial results, staged in the (then idle) Q tiles and K/V ring:
-    // unnormalised O rows (float32, padded stride) and the per-row m, l
-    static constexpr int PSTR = D + 4;
-    static constexpr int PART_BYTES = (NQ * 128 * PSTR + 2 * NQ * 128) * 4;
+    // unnormalised O (float32) and the per-row m, l.  O is stored as 16-byte
+    // pieces [query tile][32-column chunk][piece k of 8][row], so the 32 lanes
+    // of a warp (32 consecutive rows) read 512 contiguous bytes per load.
+    static constexpr int PART_BYTES = (NQ * 128 * D + 2 * NQ * 128) * 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     // + alignment slack; a 512-column tensor-memory user also claims enough
     // shared memory that no second CTA can be resident (its allocation would wait)
@@ -208,8 +209,8 @@ struct TcParams {
     // items [0, n_full) whole, CTA c taking items c, c + G, c + 2G, ...
     // (causal: every other round in reverse, so long and short items mix);
     // then each item in [n_full, items) split along K/V into `split` parts,
-    // run as the last unit of the `split` CTAs of one cluster and merged by
-    // part 0.
+    // run as the last unit of the `split` CTAs of one cluster; the parts swap
+    // partials and each merges and stores a share of O's columns.
     int items;
     int n_full;
     int split;
@@ -1074,24 +1075,51 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                 l += lo;
                 pair_sync();   // both have read it: the next unit may exchange again
             }
-            // A split item: every part but the first publishes its partial result
-            // (unnormalised O, m, l per row) in its own shared
-            // memory; the first part merges them with its own, with the same
-            // rescale as between tiles: M = max_p m_p, weights 2^(m_p - M).
             if (nkvq > 0 && ok) ok = mbar_wait(bar(S::BAR_OFULL + q), uo & 1, abort_flag, p.err, 21);
             tc_fence_after();
-            float a_own = 1.f;                 // weight of this CTA's O
-            float a_part[7];                   // weights of the other parts' O (0: nothing to add)
+            // Chunk c (32 columns) of this thread's row of O, times 1 / l, as
+            // bf16: two 32-byte stores (whole sectors) when O is 32-byte aligned.
+            const bool wide = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
+            auto store_chunk = [&](int c, const uint32_t (&o)[32], uint64_t inv2, bool store) {
+                __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * N + (store ? row : 0)) * D;
+                uint32_t w[16];
 #pragma unroll
-            for (int pp = 0; pp < 7; ++pp) a_part[pp] = 0.f;
-            float l_fin = l, m_fin = m;
-            bool parts_ok = false;             // the other parts' partials may be read
-            bool write_out = true;
-            const uint32_t sPart = sQ;         // partials live in the (now idle) Q tiles and K/V ring
-            const uint32_t part_row = sPart + ((q * 128 + row_in) * S::PSTR) * 4;
-            auto stat_addr = [&](int k) { return sPart + (NQ * 128 * S::PSTR + k * NQ * 128 + q * 128 + row_in) * 4; };
+                for (int e = 0; e < 16; ++e) {
+                    const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2);
+                    float v0, v1;
+                    f2_unpack(v, v0, v1);
+                    w[e] = pack_bf16x2(v0, v1);
+                }
+                if (store && wide) {
+#pragma unroll
+                    for (int k = 0; k < 2; ++k)
+                        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + 32 * c + 16 * k),
+                                     "r"(w[8 * k]), "r"(w[8 * k + 1]), "r"(w[8 * k + 2]), "r"(w[8 * k + 3]),
+                                     "r"(w[8 * k + 4]), "r"(w[8 * k + 5]), "r"(w[8 * k + 6]), "r"(w[8 * k + 7])
+                                     : "memory");
+                } else if (store) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(orow + 32 * c + 8 * k),
+                                     "r"(w[4 * k]), "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
+                                     : "memory");
+                }
+            };
+            bool split_unit = false;
             if constexpr (S::CAN_SPLIT) {
-                if (nparts > 1 && part > 0) {
+                if (nparts > 1) {
+                    // A split item: the parts swap their partial results
+                    // (unnormalised O, m, l per row) through shared memory across
+                    // the cluster.  Part r merges and stores the 32-column chunks c
+                    // of O with c mod nparts = r (part 0 also the LSE), with the
+                    // same rescale as between tiles: M = max_r m_r, weights
+                    // 2^(m_r - M).  Every part forms l the same way (ranks in
+                    // order), so a row's chunks share one normaliser.
+                    split_unit = true;
+                    const uint32_t sPart = sQ;   // partials live in the (now idle) Q tiles and K/V ring
+                    // piece k of chunk c of this thread's row; the row's m (k = 0) and l (k = 1)
+                    auto part_at = [&](int c, int k) { return sPart + (((q * (D / 32) + c) * 8 + k) * 128 + row_in) * 16; };
+                    auto stat_addr = [&](int k) { return sPart + (NQ * 128 * D + k * NQ * 128 + q * 128 + row_in) * 4; };
                     // The ring is reused only after every MMA of the CTA (both query
                     // tiles) has completed: the other tile's last PV may still read V.
                     mbar_wait(bar(S::BAR_DONE), 0, abort_flag, p.err, 24);
@@ -1099,13 +1127,14 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                     if (nkvq > 0) {
 #pragma unroll
                         for (int c = h * OC; c < (h + 1) * OC; ++c) {
+                            if ((c & (nparts - 1)) == part) continue;   // merged here
                             uint32_t o[32];
                             tmem_ld32(tO + 32 * c, o);
                             tmem_ld_wait();
                             reg_fence32(o);
 #pragma unroll
                             for (int k = 0; k < 8; ++k)
-                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(part_row + (32 * c + 4 * k) * 4),
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(part_at(c, k)),
                                              "r"(o[4 * k]), "r"(o[4 * k + 1]), "r"(o[4 * k + 2]), "r"(o[4 * k + 3])
                                              : "memory");
                         }
@@ -1114,101 +1143,91 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
                         asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(0)), "f"(m) : "memory");
                         asm volatile("st.shared.f32 [%0], %1;" ::"r"(stat_addr(1)), "f"(l) : "memory");
                     }
-                    mbar_arrive_remote(mapa_shared(bar(S::BAR_PART), 0));
-                    // This CTA's shared memory outlives the first part's reads: every
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+                        if (r < nparts && r != part) mbar_arrive_remote(mapa_shared(bar(S::BAR_PART), r));
+                    // This CTA's shared memory outlives the other parts' reads: every
                     // thread of every part meets at the cluster barrier at the end.
-                    write_out = false;
-                } else if (nparts > 1) {
                     // A failed wait (the error word has it) reads no partial: the
                     // merge then has only this part's keys, and the O / LSE stores
                     // below are skipped because the abort flag is set.
                     // Every part's (m, l) is read in one round trip over the
                     // cluster (all loads issued before any is used).
-                    parts_ok = mbar_wait_cluster(bar(S::BAR_PART), 0, abort_flag, p.err, 23);
-                    float mps[7], lps[7];
+                    const bool parts_ok = mbar_wait_cluster(bar(S::BAR_PART), 0, abort_flag, p.err, 23);
+                    float mr[8], lr[8];
 #pragma unroll
-                    for (int pp = 1; pp < 8; ++pp) {
-                        mps[pp - 1] = kNegInf;
-                        lps[pp - 1] = 0.f;
-                        if (parts_ok && pp < nparts) {
-                            mps[pp - 1] = ld_cluster_f32(mapa_shared(stat_addr(0), pp));
-                            lps[pp - 1] = ld_cluster_f32(mapa_shared(stat_addr(1), pp));
+                    for (int r = 0; r < 8; ++r) {
+                        mr[r] = kNegInf;
+                        lr[r] = 0.f;
+                        if (r == part) {
+                            mr[r] = m;
+                            lr[r] = l;
+                        } else if (parts_ok && r < nparts) {
+                            mr[r] = ld_cluster_f32(mapa_shared(stat_addr(0), r));
+                            lr[r] = ld_cluster_f32(mapa_shared(stat_addr(1), r));
                         }
                     }
-                    m_fin = m;
+                    float m_fin = mr[0];
 #pragma unroll
-                    for (int pp = 0; pp < 7; ++pp) m_fin = fmaxf(m_fin, mps[pp]);
-                    a_own = (m == kNegInf || m_fin == kNegInf) ? 0.f : ex2(m - m_fin);
-                    l_fin = a_own * l;
+                    for (int r = 1; r < 8; ++r) m_fin = fmaxf(m_fin, mr[r]);
+                    float a_r[8];   // weight of part r's O (0: nothing to add)
+                    float l_fin = 0.f, a_own = 0.f;
 #pragma unroll
-                    for (int pp = 0; pp < 7; ++pp) {
-                        a_part[pp] = (mps[pp] == kNegInf || m_fin == kNegInf) ? 0.f : ex2(mps[pp] - m_fin);
-                        l_fin += a_part[pp] * lps[pp];
+                    for (int r = 0; r < 8; ++r) {
+                        a_r[r] = (mr[r] == kNegInf || m_fin == kNegInf) ? 0.f : ex2(mr[r] - m_fin);
+                        l_fin = r == 0 ? a_r[0] * lr[0] : l_fin + a_r[r] * lr[r];
+                        if (r == part) a_own = a_r[r];
+                    }
+                    if (nkvq > 0) {
+                        const bool any = l_fin > 0.f;
+                        const float inv = any ? 1.f / l_fin : 0.f;
+                        const bool store = active && row < N && !*abort_flag;
+#pragma unroll
+                        for (int c = h * OC; c < (h + 1) * OC; ++c) {
+                            if ((c & (nparts - 1)) != part) continue;   // another part's chunk
+                            uint32_t o[32];
+                            tmem_ld32(tO + 32 * c, o);
+                            tmem_ld_wait();
+                            reg_fence32(o);
+                            // O = a_part O_part + sum_r a_r O_r (the other parts' O read
+                            // from their shared memory through the cluster)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a_own);
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) {
+                                const float ar = a_r[r];
+                                if (r >= nparts || r == part || ar == 0.f) continue;
+                                const uint32_t src = mapa_shared(part_at(c, 0), r);
+                                // the chunk's 8 loads are issued before the first is used
+                                float v[32];
+#pragma unroll
+                                for (int k = 0; k < 8; ++k)
+                                    ld_cluster_v4(src + 128 * 16 * k, v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(fmaf(ar, v[e], __uint_as_float(o[e])));
+                            }
+                            store_chunk(c, o, f2_pack(inv, inv), store);
+                        }
+                        if (h == 0 && part == 0 && active && p.lse != nullptr && row < N && !*abort_flag)
+                            p.lse[static_cast<size_t>(bh) * N + row] = any ? (m_fin + log2f(l_fin)) * kLn2 : kNegInf;
                     }
                 }
             }
-            if (nkvq > 0 && write_out) {
-                const bool any = l_fin > 0.f;
-                const float inv = any ? 1.f / l_fin : 0.f;
+            if (!split_unit && nkvq > 0) {
+                const bool any = l > 0.f;
+                const float inv = any ? 1.f / l : 0.f;
                 const uint64_t inv2 = f2_pack(inv, inv);
-                // this thread's row of O, 64 bytes per 32-column chunk: two
-                // 32-byte stores (whole sectors) when O is 32-byte aligned
                 const bool store = active && row < N && !*abort_flag;
-                const bool wide = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
-                __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * N + (store ? row : 0)) * D;
 #pragma unroll
                 for (int c = h * OC; c < (h + 1) * OC; ++c) {
                     uint32_t o[32];
                     tmem_ld32(tO + 32 * c, o);
                     tmem_ld_wait();
                     reg_fence32(o);
-                    if constexpr (S::CAN_SPLIT) {
-                        if (nparts > 1) {
-                            // O = a_own O_own + sum_p a_p O_p (other parts read from
-                            // their shared memory through the cluster)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a_own);
-#pragma unroll
-                            for (int pp = 1; pp < 8; ++pp) {
-                                const float ap = a_part[pp - 1];
-                                if (pp >= nparts || ap == 0.f) continue;
-                                const uint32_t src = mapa_shared(part_row + 32 * c * 4, pp);
-                                // the chunk's 8 loads are issued before the first is used
-                                float v[32];
-#pragma unroll
-                                for (int k = 0; k < 8; ++k) ld_cluster_v4(src + 16 * k, v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(fmaf(ap, v[e], __uint_as_float(o[e])));
-                            }
-                        }
-                    }
-                    uint32_t w[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2);
-                        float v0, v1;
-                        f2_unpack(v, v0, v1);
-                        w[e] = pack_bf16x2(v0, v1);
-                    }
-                    if (store && wide) {
-#pragma unroll
-                        for (int k = 0; k < 2; ++k)
-                            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
-                                             orow + 32 * c + 16 * k),
-                                         "r"(w[8 * k]), "r"(w[8 * k + 1]), "r"(w[8 * k + 2]), "r"(w[8 * k + 3]),
-                                         "r"(w[8 * k + 4]), "r"(w[8 * k + 5]), "r"(w[8 * k + 6]), "r"(w[8 * k + 7])
-                                         : "memory");
-                    } else if (store) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(orow + 32 * c + 8 * k),
-                                         "r"(w[4 * k]), "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
-                                         : "memory");
-                    }
+                    store_chunk(c, o, inv2, store);
                 }
-                if (h == 0 && active && p.lse != nullptr && row < N && !*abort_flag) {
-                    p.lse[static_cast<size_t>(bh) * N + row] = any ? (m_fin + log2f(l_fin)) * kLn2 : kNegInf;
-                }
+                if (h == 0 && active && p.lse != nullptr && row < N && !*abort_flag)
+                    p.lse[static_cast<size_t>(bh) * N + row] = any ? (m + log2f(l)) * kLn2 : kNegInf;
             }
             if (nkvq > 0) {
                 // The epilogue has read O_q: the next unit's first P V may overwrite it.
@@ -1227,7 +1246,7 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         tmem_dealloc(tmem, S::TMEM_COLS);
     }
     if constexpr (S::CAN_SPLIT) {
-        // Split item: no part exits while the first part may still read its
+        // Split item: no part exits while another part may still read its
         // shared memory.  Every thread reaches this point on every path (all
         // waits above are bounded), so the barrier always completes.
         if (p.split > 1) cluster_sync();
