@@ -227,3 +227,31 @@ def test_masked_split_tail_two_batches(eta, d):
     rows = workloads.sample_rows(B, Hh, N, 1 / 16, seed=d)
     run_case(eta, B, Hh, N, d, "bf16", False, Br=Br, Bc=Bc, mask=mask, rows=rows, seed=d)
     assert "_kvsplit2" in eta.attn_last_variant()
+
+
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("d", [64, 128])
+def test_split_tail_writes_every_element(eta, d, split):
+    """Every part of a split item merges and stores its own share of O's
+    32-column chunks (part 0 also the LSE).  With O and LSE filled with NaN
+    before the call, every element comes back finite, and sampled rows match
+    the oracle."""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    N, Br, Bc = 1000, 128, 128
+    num_qg = -(-N // (2 * Br))
+    H = _heads_for_split(nsm, num_qg, split, -(-N // Bc), False)
+    if H is None:
+        pytest.skip(f"no head count splits the tail {split} ways on {nsm} SMs")
+    q, k, v = workloads.make_qkv(1, H, N, d, "bf16", seed=40 + split)
+    dev = torch.device("cuda")
+    o = torch.full((1, H, N, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((1, H, N), float("nan"), dtype=torch.float32, device=dev)
+    eta.attn_fwd(q.to(dev), k.to(dev), v.to(dev), False, 1.0 / math.sqrt(d), Br, Bc, None, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert eta.attn_status() == eta.ATTN_OK
+    assert f"_kvsplit{split}" in eta.attn_last_variant()
+    assert not torch.isnan(o).any(), "an O element was not written"
+    assert not torch.isnan(lse).any(), "an LSE element was not written"
+    rows = workloads.sample_rows(1, H, N, 1 / 16, seed=split)
+    run_case(eta, 1, H, N, d, "bf16", False, Br=Br, Bc=Bc, rows=rows, qkv=(q, k, v))
+    assert f"_kvsplit{split}" in eta.attn_last_variant()
