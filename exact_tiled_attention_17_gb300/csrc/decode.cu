@@ -316,9 +316,11 @@ __global__ void __launch_bounds__(32 * (kDecWarps + 1)) decode_partial_kernel(co
     }
 }
 
-// one CTA per (b, h, row): merge the splits' partials.  The splits' (m, l)
-// are read in parallel and their weights 2^(m_s - M) kept in shared memory, so
-// the per-column sums over the splits issue all their loads at once.
+// one CTA per (b, h, row): merge the splits' partials.  Every split's (m, l)
+// is read in one round trip and the weights 2^(m_s - M) kept in shared
+// memory; the per-column sums over the splits load eight splits' values
+// before using the first (a dependent load per split made the merge a chain
+// of round trips), and add them in split order.
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecParams p) {
     __shared__ float wsh[kDecodeMaxSplits];
     __shared__ float red[4];
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecParams p) {
     const long long nrow = static_cast<long long>(p.BH) * p.Nq;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const float ms = t < p.splits ? p.pm[t * nrow + row] : -INFINITY;
+    const float ls = t < p.splits ? p.pl[t * nrow + row] : 0.f;
     float M = warp_max(ms);
     if (lane == 0) red[warp] = M;
     __syncthreads();
@@ -334,13 +337,20 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecParams p) {
     const float mu = (M == -INFINITY) ? 0.f : M;
     const float w = (ms == -INFINITY) ? 0.f : ex2(ms - mu);
     if (t < p.splits) wsh[t] = w;
-    float L = warp_sum(t < p.splits ? w * p.pl[t * nrow + row] : 0.f);
+    float L = warp_sum(t < p.splits ? w * ls : 0.f);
     if (lane == 0) red[warp] = L;
     __syncthreads();
     L = red[0] + red[1] + red[2] + red[3];
     for (int c = t; c < p.d; c += blockDim.x) {
         float acc = 0.f;
-        for (int s = 0; s < p.splits; ++s) acc += wsh[s] * p.po[(s * nrow + row) * p.d + c];
+        for (int s0 = 0; s0 < p.splits; s0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = s0 + u < p.splits ? p.po[((s0 + u) * nrow + row) * p.d + c] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (s0 + u < p.splits) acc += wsh[s0 + u] * v[u];
+        }
         store_out(p.O, p.bf16, row * p.d + c, L > 0.f ? acc / L : 0.f);
     }
     if (t == 0 && p.LSE) p.LSE[row] = L > 0.f ? (M + log2f(L)) * kLn2D : -INFINITY;
