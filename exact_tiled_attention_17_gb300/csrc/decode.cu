@@ -314,6 +314,9 @@ __global__ void __launch_bounds__(32 * (kDecWarps + 1)) decode_partial_kernel(co
             }
         }
     }
+    // The merge kernel (a programmatic dependent launch) may be scheduled now;
+    // it waits for this grid's completion before it reads a partial.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // one CTA per (b, h, row): merge the splits' partials.  Every split's (m, l)
@@ -324,6 +327,9 @@ __global__ void __launch_bounds__(32 * (kDecWarps + 1)) decode_partial_kernel(co
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecParams p) {
     __shared__ float wsh[kDecodeMaxSplits];
     __shared__ float red[4];
+    // Launched as a programmatic dependent of the partial kernel: wait until
+    // that grid has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long row = blockIdx.x;   // bh * Nq + i
     const long long nrow = static_cast<long long>(p.BH) * p.Nq;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -474,8 +480,22 @@ int launch_decode(const void *Q, const void *K, const void *V, void *O, float *L
     if (rc != kOk) return rc;
     if (cudaGetLastError() != cudaSuccess) return kErrCuda;
     if (p.splits > 1) {
-        decode_merge_kernel<<<static_cast<unsigned>(p.BH * Nq), 128, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+        // programmatic dependent launch: the merge grid's launch overlaps the
+        // end of the partial grid (the kernel waits for it, griddepcontrol)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(p.BH * Nq));
+        cfg.blockDim = dim3(128);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, decode_merge_kernel, p) != cudaSuccess) {
+            (void)cudaGetLastError();   // not available: an ordinary launch (the wait is then a no-op)
+            decode_merge_kernel<<<static_cast<unsigned>(p.BH * Nq), 128, 0, stream>>>(p);
+            if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+        }
     }
     return kOk;
 }
