@@ -43,6 +43,7 @@
 #include <atomic>
 #include <cstdio>
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -197,6 +198,9 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent of the prep kernel: no global
+    // memory is read or written before that grid has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp >= S::COMPUTE_WARPS) {
         // All 32 lanes run the loop with warp-uniform values; one elected lane
@@ -484,6 +488,9 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
         }
     }
 
+    // The finish kernel may be scheduled now (it waits for this grid's
+    // completion before it reads the accumulator).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     if (warp == S::WARP_MMA) {
@@ -492,56 +499,82 @@ __global__ void __launch_bounds__(BwdShape<D>::THREADS, 1)
     }
 }
 
-// One warp per (padded) query row: D_i = <dO_i, O_i>, LSE in log2 units, and
-// the row of the dQ accumulator cleared.
+// Per (padded) query row: D_i = <dO_i, O_i>, LSE in log2 units, and the row
+// of the dQ accumulator cleared.  A warp takes RPW consecutive rows of one
+// head and issues all their loads before it uses one.
+constexpr int kPrepRowsPerWarp = 4;   // divides npad (a multiple of 64)
+
 template <int D>
 __global__ void attn_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O, const __nv_bfloat16 *__restrict__ dO,
                                      const float *__restrict__ LSE, float *__restrict__ lse2,
                                      float *__restrict__ dvec, float *__restrict__ dq_acc, int BH, int N, int npad) {
+    constexpr int RPW = kPrepRowsPerWarp;
     const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (gw >= static_cast<long long>(BH) * npad) return;
-    const int bh = static_cast<int>(gw / npad);
-    const int i = static_cast<int>(gw % npad);
-    const size_t srow = static_cast<size_t>(bh) * npad + i;
-    if (i >= N) {
-        if (lane == 0) {
-            lse2[srow] = kPosInfBw;
-            dvec[srow] = 0.f;
-        }
-        return;
-    }
-    const size_t row = static_cast<size_t>(bh) * N + i;
-    constexpr int PER = D / 32;   // elements per lane (2 or 4), one vector load each
-    float acc = 0.f;
-    if constexpr (PER == 4) {
-        const uint2 ov = *reinterpret_cast<const uint2 *>(O + row * D + lane * PER);
-        const uint2 gv = *reinterpret_cast<const uint2 *>(dO + row * D + lane * PER);
-        acc = fmaf(bf16lo_to_f32(ov.x), bf16lo_to_f32(gv.x), acc);
-        acc = fmaf(bf16hi_to_f32(ov.x), bf16hi_to_f32(gv.x), acc);
-        acc = fmaf(bf16lo_to_f32(ov.y), bf16lo_to_f32(gv.y), acc);
-        acc = fmaf(bf16hi_to_f32(ov.y), bf16hi_to_f32(gv.y), acc);
-    } else {
-        const uint32_t ov = *reinterpret_cast<const uint32_t *>(O + row * D + lane * PER);
-        const uint32_t gv = *reinterpret_cast<const uint32_t *>(dO + row * D + lane * PER);
-        acc = fmaf(bf16lo_to_f32(ov), bf16lo_to_f32(gv), acc);
-        acc = fmaf(bf16hi_to_f32(ov), bf16hi_to_f32(gv), acc);
-    }
+    if (gw * RPW < static_cast<long long>(BH) * npad) {
+        const int bh = static_cast<int>(gw * RPW / npad);
+        const int i0 = static_cast<int>(gw * RPW % npad);   // the RPW rows are i0 .. i0 + RPW - 1 of head bh
+        constexpr int PER = D / 32;   // elements per lane (2 or 4), one vector load each
+        using V = typename std::conditional<PER == 4, uint2, uint32_t>::type;
+        V ov[RPW], gv[RPW];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    float *z = dq_acc + row * D + lane * PER;
-    if constexpr (PER == 4) *reinterpret_cast<float4 *>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
-    else *reinterpret_cast<float2 *>(z) = make_float2(0.f, 0.f);
-    if (lane == 0) {
-        const float l = LSE[row];
-        lse2[srow] = (l == kNegInfBw) ? kPosInfBw : l * kLog2eBw;
-        dvec[srow] = acc;
+        for (int r = 0; r < RPW; ++r) {
+            if (i0 + r < N) {
+                const size_t row = static_cast<size_t>(bh) * N + i0 + r;
+                ov[r] = *reinterpret_cast<const V *>(O + row * D + lane * PER);
+                gv[r] = *reinterpret_cast<const V *>(dO + row * D + lane * PER);
+            }
+        }
+        float acc[RPW];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            acc[r] = 0.f;
+            if (i0 + r < N) {
+                if constexpr (PER == 4) {
+                    acc[r] = fmaf(bf16lo_to_f32(ov[r].x), bf16lo_to_f32(gv[r].x), acc[r]);
+                    acc[r] = fmaf(bf16hi_to_f32(ov[r].x), bf16hi_to_f32(gv[r].x), acc[r]);
+                    acc[r] = fmaf(bf16lo_to_f32(ov[r].y), bf16lo_to_f32(gv[r].y), acc[r]);
+                    acc[r] = fmaf(bf16hi_to_f32(ov[r].y), bf16hi_to_f32(gv[r].y), acc[r]);
+                } else {
+                    acc[r] = fmaf(bf16lo_to_f32(ov[r]), bf16lo_to_f32(gv[r]), acc[r]);
+                    acc[r] = fmaf(bf16hi_to_f32(ov[r]), bf16hi_to_f32(gv[r]), acc[r]);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const size_t srow = static_cast<size_t>(bh) * npad + i0 + r;
+            if (i0 + r >= N) {
+                if (lane == 0) {
+                    lse2[srow] = kPosInfBw;
+                    dvec[srow] = 0.f;
+                }
+                continue;
+            }
+            const size_t row = static_cast<size_t>(bh) * N + i0 + r;
+            float *z = dq_acc + row * D + lane * PER;
+            if constexpr (PER == 4) *reinterpret_cast<float4 *>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
+            else *reinterpret_cast<float2 *>(z) = make_float2(0.f, 0.f);
+            if (lane == 0) {
+                const float l = LSE[row];
+                lse2[srow] = (l == kNegInfBw) ? kPosInfBw : l * kLog2eBw;
+                dvec[srow] = acc[r];
+            }
+        }
     }
+    // The main kernel (a programmatic dependent launch) may be scheduled now.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // dQ = bf16(scale * accumulator), four elements per thread.
 __global__ void attn_bwd_finish_kernel(const float4 *__restrict__ acc, uint2 *__restrict__ dq, long long n4,
                                        float scale) {
+    // a programmatic dependent of the main kernel: its reductions are complete first
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (long long k = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; k < n4;
          k += static_cast<long long>(gridDim.x) * blockDim.x) {
         const float4 a = acc[k];
@@ -607,7 +640,7 @@ int launch_bwd_d(const void *Q, const void *K, const void *V, const void *O, con
     if (!err) return kErrCuda;
 
     {
-        const long long warps = static_cast<long long>(BH) * npad;
+        const long long warps = static_cast<long long>(BH) * npad / kPrepRowsPerWarp;
         const long long blocks = (warps * 32 + 255) / 256;
         if (blocks > 0x7fffffffLL) return kErrUnsupported;
         attn_bwd_prep_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
@@ -631,15 +664,45 @@ int launch_bwd_d(const void *Q, const void *K, const void *V, const void *O, con
     p.err = err;
     const long long grid = static_cast<long long>(BH) * p.nkt;
     if (grid > 0x7fffffffLL) return kErrUnsupported;
-    kern<<<static_cast<unsigned>(grid), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p);
-    if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+    // The main and finish kernels are programmatic dependent launches: each
+    // grid's launch overlaps the end of the one before, and each waits for it
+    // (griddepcontrol.wait) before touching global memory.  An ordinary launch
+    // is the fallback.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(S::THREADS);
+        cfg.dynamicSmemBytes = S::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = pdl;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, tdk, tdv, tdq, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            kern<<<static_cast<unsigned>(grid), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdk, tdv, tdq,
+                                                                                   p);
+            if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+        }
+    }
     {
         const long long n4 = static_cast<long long>(BH) * N * D / 4;
         long long blocks = (n4 + 255) / 256;
         if (blocks > 4 * 152 * 8) blocks = 4 * 152 * 8;
-        attn_bwd_finish_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            reinterpret_cast<const float4 *>(acc), static_cast<uint2 *>(dQ), n4, scale);
-        if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cfg.attrs = pdl;
+        cfg.numAttrs = 1;
+        const float4 *a4 = reinterpret_cast<const float4 *>(acc);
+        uint2 *q2 = static_cast<uint2 *>(dQ);
+        if (cudaLaunchKernelEx(&cfg, attn_bwd_finish_kernel, a4, q2, n4, scale) != cudaSuccess) {
+            (void)cudaGetLastError();
+            attn_bwd_finish_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a4, q2, n4, scale);
+            if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+        }
     }
     return kOk;
 }
