@@ -410,6 +410,10 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         if constexpr (BSPARSE) return kv_list[jj] & 0x3FFF;
         else return kv_lo + jj;
     };
+    // Launched as a programmatic dependent of the kernel before it in the
+    // stream: no global memory is read or written before that grid has
+    // completed (the set-up above touches only this CTA's memories).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if constexpr (S::CAN_SPLIT) {
         // Parts of a split item arrive on each other's barriers: all of the
         // cluster's barriers must be initialised first.
@@ -1239,6 +1243,9 @@ __global__ void __launch_bounds__(TcShape<D, BR, BC, NQ, MASKED, BSPARSE>::THREA
         }   // work units
     }
 
+    // The next kernel in the stream may be scheduled now (it waits for this
+    // grid's completion before it touches global memory).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     if (warp == S::WARP_MMA) {
@@ -1367,13 +1374,15 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
         cfg.blockDim = dim3(S::THREADS);
         cfg.dynamicSmemBytes = S::SMEM_BYTES;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = static_cast<unsigned>(split);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p) == cudaSuccess) {
             if (split_out) *split_out = split;
             return kOk;
@@ -1385,6 +1394,20 @@ int launch_variant(const void *Q, const void *K, const void *V, void *O, float *
         grid = std::min<long long>(items, nsm);
     }
     if (split_out) *split_out = 1;
+    // a programmatic dependent launch: its launch overlaps the end of the
+    // kernel before it in the stream (an ordinary launch is the fallback)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(S::THREADS);
+    cfg.dynamicSmemBytes = S::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p) == cudaSuccess) return kOk;
+    (void)cudaGetLastError();
     kern<<<static_cast<unsigned>(grid), S::THREADS, S::SMEM_BYTES, stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
