@@ -150,6 +150,9 @@ __global__ void __launch_bounds__(32 * (kDecWarps + 1)) decode_partial_kernel(co
         abort_flag = 0u;
         fence_mbar_init();
     }
+    // Launched as a programmatic dependent of the kernel before it in the
+    // stream: no global memory is touched before that grid has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int t = threadIdx.x; t < NQ * D; t += blockDim.x) {
         float f[1];
         loadE<1>(p.Q, p.bf16, qbase + t, f);
@@ -360,6 +363,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecParams p) {
         store_out(p.O, p.bf16, row * p.d + c, L > 0.f ? acc / L : 0.f);
     }
     if (t == 0 && p.LSE) p.LSE[row] = L > 0.f ? (M + log2f(L)) * kLn2D : -INFINITY;
+    // the next call's partial kernel may be scheduled now (it waits for this grid)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <int NQ, int E>
@@ -417,7 +422,21 @@ int launch_partial(DecParams &p, cudaStream_t stream) {
             cudaSuccess)
         return kErrCuda;
     choose_splits(p, std::max(1, per_sm) * std::max(1, nsm));
-    decode_partial_kernel<NQ, E><<<dim3(p.splits, p.BH), threads, smem, stream>>>(p);
+    // a programmatic dependent launch (an ordinary launch is the fallback)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.splits), static_cast<unsigned>(p.BH));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_partial_kernel<NQ, E>, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        decode_partial_kernel<NQ, E><<<dim3(p.splits, p.BH), threads, smem, stream>>>(p);
+    }
     return kOk;
 }
 
