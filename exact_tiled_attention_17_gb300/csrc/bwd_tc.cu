@@ -509,6 +509,9 @@ __global__ void attn_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O, const 
                                      const float *__restrict__ LSE, float *__restrict__ lse2,
                                      float *__restrict__ dvec, float *__restrict__ dq_acc, int BH, int N, int npad) {
     constexpr int RPW = kPrepRowsPerWarp;
+    // a programmatic dependent of the kernel before it in the stream: no
+    // global memory is touched before that grid has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (gw * RPW < static_cast<long long>(BH) * npad) {
@@ -583,6 +586,8 @@ __global__ void attn_bwd_finish_kernel(const float4 *__restrict__ acc, uint2 *__
         w.y = pack_bf16x2(a.z * scale, a.w * scale);
         dq[k] = w;
     }
+    // the next kernel in the stream may be scheduled now (it waits for this grid)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // The float32 dQ accumulator [BH][N][D] as a tensor of 32-row boxes (no swizzle).
@@ -643,10 +648,25 @@ int launch_bwd_d(const void *Q, const void *K, const void *V, const void *O, con
         const long long warps = static_cast<long long>(BH) * npad / kPrepRowsPerWarp;
         const long long blocks = (warps * 32 + 255) / 256;
         if (blocks > 0x7fffffffLL) return kErrUnsupported;
-        attn_bwd_prep_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), LSE, lse2, dvec, acc, BH,
-            N, npad);
-        if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+        // a programmatic dependent launch, like the two kernels after it
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const __nv_bfloat16 *o16 = static_cast<const __nv_bfloat16 *>(O);
+        const __nv_bfloat16 *do16 = static_cast<const __nv_bfloat16 *>(dO);
+        if (cudaLaunchKernelEx(&cfg, attn_bwd_prep_kernel<D>, o16, do16, LSE, lse2, dvec, acc, BH, N, npad) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            attn_bwd_prep_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o16, do16, LSE, lse2, dvec,
+                                                                                     acc, BH, N, npad);
+            if (cudaGetLastError() != cudaSuccess) return kErrCuda;
+        }
     }
     BwdParams p;
     p.N = N;
