@@ -5,7 +5,11 @@
  * C linkage and takes plain pointers and sizes.  No entry point allocates
  * device memory: tensors and workspaces are owned by the caller.  Work is
  * enqueued on the caller's stream (a cudaStream_t passed as void*; NULL means
- * the legacy default stream) on the current device.
+ * the legacy default stream) on the current device.  The tensor-core forward,
+ * the backward and the decode kernels are programmatic dependent launches:
+ * each may be scheduled while the kernel before it in the stream finishes,
+ * but reads or writes no global memory until that grid has completed, so
+ * stream order holds as for an ordinary launch.
  *
  * Errors are reported synchronously through the return value and nothing is
  * launched when an argument is rejected.  There is no CPU fallback and no

@@ -255,3 +255,48 @@ def test_split_tail_writes_every_element(eta, d, split):
     rows = workloads.sample_rows(1, H, N, 1 / 16, seed=split)
     run_case(eta, 1, H, N, d, "bf16", False, Br=Br, Bc=Bc, rows=rows, qkv=(q, k, v))
     assert f"_kvsplit{split}" in eta.attn_last_variant()
+
+
+def test_dependent_launch_chain_matches_synchronised_calls(eta):
+    """The forward, backward and decode kernels are programmatic dependent
+    launches: each waits for the grid before it in the stream before it
+    touches global memory.  A chain of calls that each read the previous
+    call's output, enqueued back to back, gives bitwise the same O, LSE, dK
+    and dV as the same calls with a synchronize after each (dQ, reduced with
+    float atomics in any order, within rounding), and the chain's first
+    output matches the oracle."""
+    B, H, N, d = 1, 4, 1000, 128
+    q, k, v = workloads.make_qkv(B, H, N, d, "bf16", seed=77)
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    scale = 1.0 / math.sqrt(d)
+
+    def chain(sync):
+        def s():
+            if sync:
+                torch.cuda.synchronize()
+        o1, l1 = eta.attn_fwd(qd, kd, vd, False, scale)
+        s()
+        o2, l2 = eta.attn_fwd(o1, kd, vd, True, scale)     # the last output as the queries
+        s()
+        o3, l3 = eta.attn_fwd(o2, kd, o1, False, scale)    # and as the values
+        s()
+        dq, dk, dv = eta.attn_bwd(o2, kd, o1, o3, o2, l3, False, scale)
+        s()
+        od, ld = eta.attn_decode_fwd(dk[:, :, N - 4:].contiguous(), kd, dv, True, scale)
+        s()
+        o4, l4 = eta.attn_fwd(dv, dk, o3, False, scale)
+        torch.cuda.synchronize()
+        assert eta.attn_status() == eta.ATTN_OK
+        return [t.clone() for t in (o1, l1, o2, l2, o3, l3, dq, dk, dv, od, ld, o4, l4)]
+
+    a = chain(False)
+    b = chain(True)
+    names = ["o1", "l1", "o2", "l2", "o3", "l3", "dq", "dk", "dv", "od", "ld", "o4", "l4"]
+    for name, x, y in zip(names, a, b):
+        if name == "dq":
+            assert torch.allclose(x.float(), y.float(), rtol=0, atol=1e-2 * max(1.0, y.float().abs().max().item()))
+        else:
+            assert torch.equal(x, y), f"{name} differs between the chained and the synchronised calls"
+    rows = workloads.sample_rows(B, H, N, 1 / 16, seed=77)
+    run_case(eta, B, H, N, d, "bf16", False, rows=rows, qkv=(q, k, v))
