@@ -213,3 +213,46 @@ def test_host_entry_sizes_and_rejection(lib):
     assert host(Bc=96) == -2
     assert host(dtype=2) == -2
     assert host(dtype=0, Br=128) == -2
+
+
+def test_decode_sizes_and_rejection(lib):
+    """attn_decode_fwd: the workspace holds the partial results of up to 128
+    key splits; argument errors are returned before anything is launched
+    (fake, never dereferenced pointers)."""
+    vp = ctypes.c_void_p
+    ws_size = lib.attn_decode_workspace_size
+    ws_size.restype = ctypes.c_size_t
+    ws_size.argtypes = [ctypes.c_int] * 4
+    # per split and row: m, l and d partial sums, float32
+    assert ws_size(1, 32, 1, 128) == 128 * 32 * 1 * (2 + 128) * 4
+    assert ws_size(2, 8, 4, 64) == 128 * 16 * 4 * (2 + 64) * 4
+    assert ws_size(0, 1, 1, 64) == 0
+    f = lib.attn_decode_fwd
+    f.restype = ctypes.c_int
+    f.argtypes = [vp] * 5 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]
+    p, big = vp(256), 1 << 30
+
+    def dec(**kw):
+        a = dict(Q=p, K=p, V=p, O=p, B=1, H=1, Nq=1, Nk=64, d=64, causal=0, scale=0.125, dtype=1, mask=None,
+                 ws=p, ws_bytes=big)
+        a.update(kw)
+        return f(a["Q"], a["K"], a["V"], a["O"], None, a["B"], a["H"], a["Nq"], a["Nk"], a["d"], a["causal"],
+                 a["scale"], a["dtype"], a["mask"], a["ws"], a["ws_bytes"], None)
+
+    assert dec(Q=None) == -1
+    assert dec(Nq=0) == -1
+    assert dec(Nk=-1) == -1
+    assert dec(scale=0.0) == -1
+    assert dec(scale=float("inf")) == -1
+    assert dec(causal=2) == -1
+    assert dec(causal=1, Nq=8, Nk=4) == -1          # causal needs Nq <= Nk
+    assert dec(dtype=7) == -1
+    assert dec(dtype=2) == -2                       # float64: bf16 or float32 only
+    assert dec(Nq=9) == -2                          # at most 8 new rows
+    assert dec(d=48) == -2                          # d a multiple of 32, at most 128
+    assert dec(d=160) == -2
+    assert dec(K=vp(264)) == -1                     # not 16-byte aligned
+    assert dec(mask=vp(258)) == -1                  # not 4-byte aligned
+    assert dec(ws=None) == -3
+    assert dec(ws_bytes=100) == -3
+    assert dec(ws=vp(264)) == -3                    # not 16-byte aligned
