@@ -256,3 +256,45 @@ def test_decode_sizes_and_rejection(lib):
     assert dec(ws=None) == -3
     assert dec(ws_bytes=100) == -3
     assert dec(ws=vp(264)) == -3                    # not 16-byte aligned
+
+
+def test_emulation_rejection(lib):
+    """attn_emul_fwd / attn_emul_round: argument errors are returned before
+    anything is launched (fake, never dereferenced pointers); n = 0 rounds
+    nothing and returns ATTN_OK."""
+    vp = ctypes.c_void_p
+    f = lib.attn_emul_fwd
+    f.restype = ctypes.c_int
+    f.argtypes = [vp, vp, vp, ctypes.c_int, vp] + [ctypes.c_int] * 5 + [ctypes.c_float, vp] + [ctypes.c_int] * 4 + \
+                 [vp, ctypes.c_longlong, vp]
+    p = vp(256)
+    BASELINE, TILED = 0, 1
+
+    def emul(**kw):
+        a = dict(Q=p, dtype=1, O=p, N=8, d=64, causal=0, scale=0.125, mask=None, algo=TILED, Bc=4, mb=7, eb=8,
+                 rows=None, nrows=0)
+        a.update(kw)
+        return f(a["Q"], p, p, a["dtype"], a["O"], 1, 1, a["N"], a["d"], a["causal"], a["scale"], a["mask"],
+                 a["algo"], a["Bc"], a["mb"], a["eb"], a["rows"], a["nrows"], None)
+
+    assert emul(Q=None) == -1
+    assert emul(N=0) == -1
+    assert emul(scale=-1.0) == -1
+    assert emul(causal=5) == -1
+    assert emul(dtype=9) == -1
+    assert emul(algo=4) == -1
+    assert emul(mb=0) == -1 and emul(mb=53) == -1
+    assert emul(eb=1) == -1 and emul(eb=12) == -1
+    assert emul(rows=p, nrows=-1) == -1
+    assert emul(Bc=0) == -1
+    assert emul(d=129) == -2
+    assert emul(mask=vp(258)) == -1                 # not 4-byte aligned
+    assert emul(O=vp(260)) == -1                    # not 8-byte aligned
+    g = lib.attn_emul_round
+    g.restype = ctypes.c_int
+    g.argtypes = [vp, vp, ctypes.c_longlong, ctypes.c_int, ctypes.c_int, vp]
+    assert g(None, p, 4, 7, 8, None) == -1
+    assert g(p, p, -1, 7, 8, None) == -1
+    assert g(p, p, 4, 0, 8, None) == -1
+    assert g(p, vp(260), 4, 7, 8, None) == -1
+    assert g(p, p, 0, 7, 8, None) == 0               # nothing to round
